@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled quantization hot path on one GB300 per rank.
+
+One step = one pass of the hot path over the NVFP4 dense workload
+(BF16 M=8192 x K=7168, N(0,1) x per-row LogNormal(0,1) with 0.1% x50
+outliers, tensor_sf = 448*6/global amax): ``bsq_quantize`` (packed E2M1 +
+E4M3 scales in the 5D TCGEN layout) followed by ``bsq_scales_interleave`` of
+the rank-2 form of the result's scales.  The metric is GB/s over the
+algorithmic bytes (BF16 in + packed out + scale bytes; 2 bytes per scale for
+the reinterleave), with the inputs resident in HBM and L2 flushed (256 MiB
+write) before every step.  Kernels are timed with CUDA events on the stream
+they are launched on.
+
+Also reported on the same JSON line: ``e2e`` (the same metric through the
+Python API with pinned host buffers, host<->device copies inside the timed
+region), ``roofline`` for the dominant kernel (dense quantize), ``clocks``
+sampled with nvidia-smi during the timed region, ``cpu_baseline`` (the CPU
+oracle on a bounded sample, rank 0 at N=1) and ``workloads`` (the other
+shapes: NVFP4 128x256, MXFP8/MXFP4 16384x4096, grouped NVFP4 prefill, grouped
+decode in microseconds per k_tiles_per_block).
+
+``--impl reference`` times the CPU oracle itself on the same workload, one
+bounded sample per step.
+
+Multi-GPU: launched under torchrun, every rank quantizes its own batch of the
+same shape on its own GPU (weak scaling, no collective on the data path); the
+step time is the max over ranks and ``value`` counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "quantize GB/s (bytes in+out) and % of GB300 HBM peak; grouped decode µs"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+CSRC = os.path.join(ROOT, "fp8_activation_quantization_bsq_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dense_nvfp4_M8192_K7168.traffic.json")
+REF_SAMPLE_ROWS = 256
+CPU_BASELINE_ROWS = 2048
+
+
+# ----------------------------------------------------------------- helpers --
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(CSRC, "*.cu*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dense kernel from the committed ncu summary,
+    or None when missing or taken on different kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_sha256") != source_digest():
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, kept only inside a window."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.06]
+        note = "samples inside the timed region"
+        if not inside and self.rows:
+            # the region was shorter than the sampling period: take the nearest sample
+            inside = [min(self.rows, key=lambda tr: abs(tr[0] - (t0 + t1) / 2))[1]]
+            note = "timed region shorter than the 50 ms sampling period: nearest sample"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "note": note}
+
+
+def to_dev_bf16(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def rank2_from_5d(scales5d, M, S):
+    """Torch view of a 5D scale buffer as (M, S) row-major bytes (setup only)."""
+    Mt, Kt = -(-M // 128), -(-S // 4)
+    v = scales5d[: Mt * Kt * 512].view(Mt, Kt, 32, 4, 4).permute(0, 3, 2, 1, 4)
+    return v.reshape(Mt * 128, Kt * 4)[:M, :S].contiguous()
+
+
+def dense_bytes(fmt: str, M: int, K: int) -> int:
+    sf = 16 if fmt == "nvfp4" else 32
+    out = M * (K if fmt == "mxfp8" else K // 2)
+    return M * K * 2 + out + M * (K // sf)
+
+
+# --------------------------------------------------------------- GPU timing --
+
+def time_events(fn, reps: int, flush=None):
+    """Mean / min device ms of fn() over reps, CUDA events on the current
+    stream, L2 flushed (outside the events) before each rep."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i, (a, b) in enumerate(evs):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(ms), min(ms)
+
+
+def extra_workloads(bsq, device, flush, peak):
+    """The other shapes, reported for context (not the headline)."""
+    import torch
+    import workloads as wl
+    res = {}
+    reps = 30
+
+    c = wl.config_dense_nvfp4_small()
+    x = to_dev_bf16(c["x_bits"], device)
+    out, sc = bsq.quantize(x, "nvfp4", float(c["tensor_sf"]))
+    mean, mn = time_events(lambda: bsq.quantize(x, "nvfp4", float(c["tensor_sf"]), out=out, scales=sc), reps, flush)
+    res["nvfp4_dense_M128_K256"] = {"us": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
+                                    "GB_s": round(dense_bytes("nvfp4", 128, 256) / (mean * 1e6), 1)}
+
+    c = wl.config_dense_mx_wide()
+    x = to_dev_bf16(c["x_bits"], device)
+    del c
+    for fmt in ("mxfp8", "mxfp4"):
+        out, sc = bsq.quantize(x, fmt)
+        mean, mn = time_events(lambda: bsq.quantize(x, fmt, out=out, scales=sc), reps, flush)
+        b = dense_bytes(fmt, 16384, 4096)
+        res[f"{fmt}_dense_M16384_K4096"] = {"GB_s": round(b / (mean * 1e6), 1), "us": round(mean * 1e3, 2),
+                                            "frac_of_hbm": round(b / (mean * 1e6) / peak, 3)}
+        del out, sc
+    del x
+
+    def grouped(d, fmt, kt, label, unique_rows):
+        xg = to_dev_bf16(d["x_bits"], device)
+        u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
+        ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
+        eid = torch.from_numpy(d["expert_ids"]).to(device)
+        sf = torch.from_numpy(d["sf_tensor"]).to(device)
+        ridx = torch.from_numpy(d["row_indices"]).to(device)
+        out, sc = bsq.grouped_quantize(xg, fmt, ro, so, eid, sf if fmt == "nvfp4" else None, ridx,
+                                       total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"],
+                                       k_tiles_per_block=kt)
+        fn = lambda: bsq.grouped_quantize(xg, fmt, ro, so, eid, sf if fmt == "nvfp4" else None, ridx,
+                                          total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"],
+                                          k_tiles_per_block=kt, out=out, scales=sc)
+        mean, mn = time_events(fn, reps, flush)
+        K = d["K"]
+        sfv = 16 if fmt == "nvfp4" else 32
+        kt_cols = -(-(K // sfv) // 4) * 4
+        b = (unique_rows * K * 2 + d["total_rows"] * (K if fmt == "mxfp8" else K // 2)
+             + d["total_rows"] * kt_cols + d["row_indices"].nbytes + d["row_offsets"].nbytes
+             + d["scales_offsets"].nbytes + d["expert_ids"].nbytes
+             + (d["sf_tensor"].nbytes if fmt == "nvfp4" else 0))
+        return mean, mn, b
+
+    d = wl.config_grouped_prefill()
+    uniq = int(np.unique(d["row_indices"]).size)
+    for kt in (8,):
+        mean, mn, b = grouped(d, "nvfp4", kt, "prefill", uniq)
+        res[f"nvfp4_grouped_prefill_T4096_K7168_kt{kt}"] = {
+            "GB_s": round(b / (mean * 1e6), 1), "us": round(mean * 1e3, 2),
+            "frac_of_hbm": round(b / (mean * 1e6) / peak, 3), "algorithmic_bytes": b,
+            "logical_input_bytes": d["total_rows"] * d["K"] * 2}
+    del d
+    for fmt in ("nvfp4", "mxfp8"):
+        for K in (7168, 2048):
+            d = wl.config_grouped_decode(K=K, fmt=fmt)
+            uniq = int(np.unique(d["row_indices"]).size)
+            for kt in (1, 2, 4, 8):
+                mean, mn, b = grouped(d, fmt, kt, "decode", uniq)
+                res[f"{fmt}_grouped_decode_T64_K{K}_kt{kt}"] = {"us": round(mean * 1e3, 2),
+                                                               "us_min": round(mn * 1e3, 2)}
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import fp8_activation_quantization_bsq_gb300 as bsq
+    import workloads as wl
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device() if world == 1 else local_rank)
+    torch.cuda.set_device(device)
+    bsq.lib()
+
+    c = wl.config_dense_nvfp4_large(seed=1 + rank)
+    M, K, tsf = c["M"], c["K"], float(c["tensor_sf"])
+    S = K // 16
+    x = to_dev_bf16(c["x_bits"], device)
+    out = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+    sc = torch.empty(bsq.scales5d_bytes("nvfp4", M, K), dtype=torch.uint8, device=device)
+    bsq.quantize(x, "nvfp4", tsf, out=out, scales=sc)
+    torch.cuda.synchronize()
+    sc2d = rank2_from_5d(sc, M, S)                       # rank-2 copy of the result's scales
+    sc5 = torch.empty_like(sc)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    q_bytes = dense_bytes("nvfp4", M, K)
+    il_bytes = 2 * M * S
+    step_bytes = q_bytes + il_bytes
+
+    def step(ev3, i):
+        flush.fill_(i & 0xFF)                            # evict L2 before the step
+        ev3[0].record(stream)
+        bsq.quantize(x, "nvfp4", tsf, out=out, scales=sc)
+        ev3[1].record(stream)
+        bsq.scales_interleave(sc2d, out=sc5)
+        ev3[2].record(stream)
+
+    mk = lambda: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+    for i in range(args.warmup):
+        step(mk(), i)
+    torch.cuda.synchronize()
+
+    evs = [mk() for _ in range(args.steps)]
+    sampler = ClockSampler(device.index) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        step(evs[i], i)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    clocks = sampler.stop(t0, t1) if sampler else None
+
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    il_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms_local = statistics.mean(a + b for a, b in zip(q_ms, il_ms))
+    step_ms = max_over_ranks(step_ms_local, world)
+    q_mean = max_over_ranks(statistics.mean(q_ms), world)
+    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    x_h = torch.from_numpy(np.ascontiguousarray(c["x_bits"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    sc2d_h = sc2d.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.uint8).pin_memory()
+    sc_h = torch.empty(sc.shape, dtype=torch.uint8).pin_memory()
+    sc5_h = torch.empty(sc5.shape, dtype=torch.uint8).pin_memory()
+    sc2d_d = torch.empty_like(sc2d)
+    h2d = x_h.numel() * 2 + sc2d_h.numel()
+    d2h = out_h.numel() + sc_h.numel() + sc5_h.numel()
+
+    def e2e_step(a, b, i):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        x.copy_(x_h, non_blocking=True)
+        sc2d_d.copy_(sc2d_h, non_blocking=True)
+        bsq.quantize(x, "nvfp4", tsf, out=out, scales=sc)
+        bsq.scales_interleave(sc2d_d, out=sc5)
+        out_h.copy_(out, non_blocking=True)
+        sc_h.copy_(sc, non_blocking=True)
+        sc5_h.copy_(sc5, non_blocking=True)
+        b.record(stream)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), i)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 50))
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    barrier(world)
+    for i, (a, b) in enumerate(ee):
+        e2e_step(a, b, i)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ee), world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = hbm_peak()
+    achieved = q_bytes / (q_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded NumPy PCG64; no dataset)",
+        "config": {"workload": "nvfp4_dense_quantize_M8192_K7168+scales_interleave",
+                   "format": "nvfp4", "M": M, "K": K, "tensor_sf": tsf,
+                   "bytes_per_step": step_bytes, "quantize_bytes": q_bytes, "interleave_bytes": il_bytes,
+                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
+                   "parallelism": f"replicas x{world} (each rank its own batch)"},
+        "hbm_frac": round(value / world / peak, 4),
+        "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "roofline": {"bound": "hbm", "kernel": "dense_quant_tma_kernel<NVFP4>",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6800 GB/s", "us_per_launch": round(q_mean * 1e3, 3)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(c, tsf)
+    if not args.no_extra:
+        line["workloads"] = extra_workloads(bsq, device, flush, peak)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample_step(c, tsf, rows):
+    """One pass of the CPU oracle over ``rows`` rows of the workload:
+    quantize (rank-2 scales + 5D) and reinterleave; returns the bytes done."""
+    import oracle
+    bits = c["x_bits"][:rows]
+    packed, s2 = oracle.quantize_rank2("nvfp4", bits, tsf)
+    oracle.scales_to_5d(s2)
+    oracle.scales_interleave(s2, rows, s2.shape[1], s2.shape[1])
+    return dense_bytes("nvfp4", rows, c["K"]) + 2 * rows * (c["K"] // 16)
+
+
+def cpu_baseline(c, tsf):
+    t0 = time.perf_counter()
+    done = 0
+    for r0 in range(0, CPU_BASELINE_ROWS, 512):
+        sub = dict(c)
+        sub["x_bits"] = c["x_bits"][r0:r0 + 512]
+        done += oracle_sample_step(sub, tsf, 512)
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {CPU_BASELINE_ROWS} of 8192 rows (4 chunks of 512), quantize + 5D + "
+                      f"interleave, NumPy single-threaded; {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import workloads as wl
+    c = wl.config_dense_nvfp4_large()
+    tsf = np.float32(c["tensor_sf"])
+    for _ in range(args.warmup):
+        oracle_sample_step(c, tsf, REF_SAMPLE_ROWS)
+    times, done = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        done = oracle_sample_step(c, tsf, REF_SAMPLE_ROWS)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = done / (ms * 1e-3) / 1e9
+    sample = f"first {REF_SAMPLE_ROWS} of 8192 rows per step (quantize + 5D + interleave), NumPy single-threaded"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded NumPy PCG64; no dataset)",
+            "config": {"workload": "nvfp4_dense_quantize_M8192_K7168+scales_interleave",
+                       "format": "nvfp4", "M": 8192, "K": 7168, "sample_rows": REF_SAMPLE_ROWS},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the context workloads")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

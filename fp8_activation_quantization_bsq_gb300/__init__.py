@@ -1,0 +1,188 @@
+"""Block-scaled BF16 -> NVFP4 / MXFP4 / MXFP8 quantization for NVIDIA GB300.
+
+Thin Python binding of ``libbsq`` (C ABI in ``include/bsq.h``): it turns
+torch tensors into pointers and sizes, allocates missing outputs with torch,
+passes torch's current CUDA stream and raises on a non-zero status.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+path.  The binding fails loudly when ``libbsq.so`` has not been built
+(``python -m fp8_activation_quantization_bsq_gb300._build`` or
+``__graft_entry__.build()``).
+
+Operations (Modular "block_scaled_quantization" pages):
+  quantize            -- quantize_dynamic_block_scaled / quantize_dynamic_scaled_fp4fp8
+  grouped_quantize    -- grouped_quantize_dynamic_scaled_fp4_async(_kernel)
+  scales_interleave   -- block_scales_interleave(_fp4)(_kernel)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB_PATH
+
+__all__ = ["FORMATS", "lib", "BsqError", "block_size", "packed_row_bytes", "scales5d_bytes",
+           "quantize", "grouped_quantize", "scales_interleave", "device_error", "status_string"]
+
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
+
+_c_i32, _c_i64, _c_f32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+
+_SIGNATURES = {
+    "bsq_version": (_c_i32, []),
+    "bsq_status_string": (ctypes.c_char_p, [_c_i32]),
+    "bsq_block_size": (_c_i32, [_c_i32]),
+    "bsq_packed_row_bytes": (_c_i64, [_c_i32, _c_i64]),
+    "bsq_scales5d_bytes": (_c_i64, [_c_i32, _c_i64, _c_i64]),
+    "bsq_quantize": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_f32, _c_p]),
+    "bsq_grouped_quantize": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p,
+                                      _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_p,
+                                      _c_i32, _c_p]),
+    "bsq_scales_interleave": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
+    "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libbsq.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbsq is not built ({LIB_PATH} missing); build it with "
+                               "python -m fp8_activation_quantization_bsq_gb300._build")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+class BsqError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)}")
+        self.code = code
+
+
+def status_string(code: int) -> str:
+    return lib().bsq_status_string(code).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise BsqError(code, what)
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def block_size(fmt) -> int:
+    return lib().bsq_block_size(_fmt(fmt))
+
+
+def packed_row_bytes(fmt, K: int) -> int:
+    return lib().bsq_packed_row_bytes(_fmt(fmt), K)
+
+
+def scales5d_bytes(fmt, rows: int, K: int) -> int:
+    return lib().bsq_scales5d_bytes(_fmt(fmt), rows, K)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def quantize(x: torch.Tensor, fmt, tensor_sf: float = 1.0, out=None, scales=None, stream=None):
+    """Quantize an (M, K) BF16 CUDA tensor (unit inner stride).
+
+    Returns (packed uint8 (M, packed_row_bytes), scales uint8 [scales5d_bytes])
+    with the scales in the 5D TCGEN layout.
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    f = _fmt(fmt)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, packed_row_bytes(f, K)), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(scales5d_bytes(f, M, K), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().bsq_quantize(f, _ptr(x), M, K, x.stride(0) if M else K, _ptr(out), _ptr(scales),
+                                float(tensor_sf), _stream(x.device, stream))
+    _check(rc, "bsq_quantize")
+    return out, scales
+
+
+def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_ids,
+                     sf_tensor=None, row_indices=None, total_rows: int | None = None,
+                     total_scale_rows: int | None = None, k_tiles_per_block: int = 1,
+                     out=None, scales=None, stream=None):
+    """Grouped per-expert quantize of the (in_rows, K) BF16 CUDA tensor ``x``.
+
+    ``row_offsets`` / ``scales_offsets`` are uint32 (stored as torch.int32
+    bit patterns or uint32) CUDA tensors of G+1 entries, ``expert_ids`` int32
+    [G], ``sf_tensor`` float32 [num_experts] (NVFP4), ``row_indices`` int32 or
+    None.  ``total_rows`` / ``total_scale_rows`` size the outputs (required
+    when ``out`` / ``scales`` are not given).
+    Returns (packed uint8 (total_rows, packed_row_bytes), scales uint8).
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    f = _fmt(fmt)
+    in_rows, K = x.shape
+    G = expert_ids.numel()
+    if total_rows is None:
+        if out is None:
+            raise ValueError("total_rows is required when out is not given")
+        total_rows = out.shape[0]
+    if total_scale_rows is None:
+        raise ValueError("total_scale_rows is required")
+    if out is None:
+        out = torch.empty((total_rows, packed_row_bytes(f, K)), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(scales5d_bytes(f, total_scale_rows, K), dtype=torch.uint8, device=x.device)
+    num_experts = sf_tensor.numel() if sf_tensor is not None else 0
+    with torch.cuda.device(x.device):
+        rc = lib().bsq_grouped_quantize(
+            f, _ptr(x), in_rows, K, x.stride(0) if in_rows else K, _ptr(row_offsets),
+            _ptr(scales_offsets), _ptr(expert_ids), _ptr(sf_tensor), num_experts,
+            _ptr(row_indices), G, total_rows, total_scale_rows, _ptr(out), _ptr(scales),
+            k_tiles_per_block, _stream(x.device, stream))
+    _check(rc, "bsq_grouped_quantize")
+    return out, scales
+
+
+def scales_interleave(scales2d: torch.Tensor, out=None, stream=None):
+    """Rank-2 (M, S) uint8 CUDA scales (unit inner stride) -> 5D layout."""
+    if scales2d.dtype != torch.uint8 or scales2d.dim() != 2 or not scales2d.is_cuda or \
+            (scales2d.shape[1] > 1 and scales2d.stride(1) != 1):
+        raise ValueError("scales2d must be a 2-D uint8 CUDA tensor with unit inner stride")
+    M, S = scales2d.shape
+    if out is None:
+        nbytes = -(-M // 128) * -(-S // 4) * 512
+        out = torch.empty(nbytes, dtype=torch.uint8, device=scales2d.device)
+    with torch.cuda.device(scales2d.device):
+        rc = lib().bsq_scales_interleave(_ptr(scales2d), M, S, scales2d.stride(0) if M else S,
+                                         _ptr(out), _stream(scales2d.device, stream))
+    _check(rc, "bsq_scales_interleave")
+    return out
+
+
+def device_error(device=None, stream=None) -> int:
+    """Synchronize and read-and-clear the device's error word (0 = none)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    code = _c_i32(0)
+    with torch.cuda.device(device):
+        rc = lib().bsq_device_error(_stream(device, stream), ctypes.byref(code))
+    _check(rc, "bsq_device_error")
+    return code.value

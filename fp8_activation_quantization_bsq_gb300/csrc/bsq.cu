@@ -1,0 +1,283 @@
+// libbsq: host side of the C ABI declared in include/bsq.h -- argument
+// validation, launch geometry, the TMA descriptor of the dense kernel, and the
+// per-device error word.  All compute runs in the kernels of dense_quant.cuh,
+// grouped_quant.cuh and interleave.cuh.
+#include "bsq.h"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "dense_quant.cuh"
+#include "device_common.cuh"
+#include "grouped_quant.cuh"
+#include "interleave.cuh"
+
+namespace {
+
+using namespace bsq;
+
+constexpr int kDenseStages = 3;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int dense_ctas_per_sm[3] = {0, 0, 0};
+};
+
+std::mutex g_mu;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+bool g_encode_tried = false;
+
+inline bool fmt_ok(int32_t f) { return f == BSQ_NVFP4 || f == BSQ_MXFP4 || f == BSQ_MXFP8; }
+inline int sf_of(int32_t f) { return f == BSQ_NVFP4 ? 16 : 32; }
+inline int atom_cols_of(int32_t f) { return 4 * sf_of(f); }
+inline int64_t row_bytes_of(int32_t f, int64_t K) { return f == BSQ_MXFP8 ? K : K / 2; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int FMT>
+void dense_kernel_setup(int fidx, DeviceInfo& d) {
+  auto k = dense_quant_tma_kernel<FMT, kDenseStages>;
+  const int smem = dense_smem_bytes<kDenseStages>();
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int n = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kDenseThreads, smem);
+  d.dense_ctas_per_sm[fidx] = n > 0 ? n : 1;
+}
+
+// Per-device constants, computed once with the device current.
+bsq_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BSQ_ERR_CUDA;
+    dense_kernel_setup<kNVFP4>(0, d);
+    dense_kernel_setup<kMXFP4>(1, d);
+    dense_kernel_setup<kMXFP8>(2, d);
+    if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return BSQ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode_tiled;
+}
+
+template <int FMT>
+bsq_status launch_dense(const void* in, int64_t M, int64_t K, int64_t ld_in, void* out,
+                        void* scales, float tsf, cudaStream_t stream) {
+  DeviceInfo* d = nullptr;
+  if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+  auto enc = encode_tiled();
+  if (!enc) return BSQ_ERR_CUDA;
+
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld_in) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kDenseBoxCols),
+                             static_cast<cuuint32_t>(kDenseTileRows)};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(in), gdim, gstride, box,
+          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return BSQ_ERR_CUDA;
+
+  DenseArgs a;
+  a.out = static_cast<uint8_t*>(out);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.out_ld = row_bytes_of(FMT, K);
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.tiles_k = static_cast<int>(ceil_div(K, kDenseTileCols));
+  a.num_tiles = static_cast<int>(ceil_div(M, kDenseTileRows) * a.tiles_k);
+  a.kt_atoms = static_cast<int>(ceil_div(K, atom_cols_of(FMT)));
+  a.vec32 = (a.out_ld % 32 == 0) && aligned(out, 32);
+  a.tsf = tsf;
+
+  const int fidx = FMT;
+  const int64_t resident = static_cast<int64_t>(d->sm_count) * d->dense_ctas_per_sm[fidx];
+  const int grid = static_cast<int>(a.num_tiles < resident ? a.num_tiles : resident);
+  dense_quant_tma_kernel<FMT, kDenseStages>
+      <<<grid, kDenseThreads, dense_smem_bytes<kDenseStages>(), stream>>>(map, a);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+template <int FMT, int KT>
+bsq_status launch_grouped_kt(const GroupedArgs& a, int64_t tiles, cudaStream_t stream) {
+  const int64_t chunks = ceil_div(a.kt_atoms, KT);
+  if (chunks > 65535) return BSQ_ERR_SHAPE;
+  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
+  grouped_quant_kernel<FMT, KT><<<grid, kGroupedThreads, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+template <int FMT>
+bsq_status launch_grouped(const GroupedArgs& a, int64_t tiles, int kt, cudaStream_t stream) {
+  switch (kt) {
+    case 1: return launch_grouped_kt<FMT, 1>(a, tiles, stream);
+    case 2: return launch_grouped_kt<FMT, 2>(a, tiles, stream);
+    case 4: return launch_grouped_kt<FMT, 4>(a, tiles, stream);
+    default: return launch_grouped_kt<FMT, 8>(a, tiles, stream);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bsq_version(void) { return (1 << 16) | 0; }
+
+const char* bsq_status_string(int32_t s) {
+  switch (s) {
+    case BSQ_OK: return "BSQ_OK";
+    case BSQ_ERR_NULL: return "BSQ_ERR_NULL: a required pointer is NULL";
+    case BSQ_ERR_SHAPE: return "BSQ_ERR_SHAPE: invalid size or stride";
+    case BSQ_ERR_ALIGN: return "BSQ_ERR_ALIGN: misaligned pointer or stride";
+    case BSQ_ERR_VALUE: return "BSQ_ERR_VALUE: invalid scalar argument or device metadata";
+    case BSQ_ERR_CUDA: return "BSQ_ERR_CUDA: a CUDA call failed";
+    case BSQ_ERR_TIMEOUT: return "BSQ_ERR_TIMEOUT: a bounded device wait expired";
+    default: return "unknown bsq status";
+  }
+}
+
+int32_t bsq_block_size(int32_t fmt) { return fmt_ok(fmt) ? sf_of(fmt) : 0; }
+
+int64_t bsq_packed_row_bytes(int32_t fmt, int64_t K) {
+  if (!fmt_ok(fmt) || K < 0) return 0;
+  return row_bytes_of(fmt, K);
+}
+
+int64_t bsq_scales5d_bytes(int32_t fmt, int64_t rows, int64_t K) {
+  if (!fmt_ok(fmt) || rows < 0 || K < 0) return 0;
+  return ceil_div(rows, 128) * ceil_div(K / sf_of(fmt), 4) * 512;
+}
+
+int32_t bsq_quantize(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in, void* out,
+                     void* scales, float tensor_sf, void* stream) {
+  if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
+  if (M < 0 || K < 0 || K % 32 != 0 || M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return BSQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return BSQ_OK;
+  if (ld_in < K) return BSQ_ERR_SHAPE;
+  if (ceil_div(M, 128) * ceil_div(K, 128) >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  if (!in || !out || !scales) return BSQ_ERR_NULL;
+  if (!aligned(in, 16) || !aligned(out, 16) || !aligned(scales, 16) || ld_in % 8 != 0)
+    return BSQ_ERR_ALIGN;
+  if (fmt == BSQ_NVFP4 && !(std::isfinite(tensor_sf) && tensor_sf > 0.0f)) return BSQ_ERR_VALUE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (fmt) {
+    case BSQ_NVFP4: return launch_dense<kNVFP4>(in, M, K, ld_in, out, scales, tensor_sf, st);
+    case BSQ_MXFP4: return launch_dense<kMXFP4>(in, M, K, ld_in, out, scales, 1.0f, st);
+    default: return launch_dense<kMXFP8>(in, M, K, ld_in, out, scales, 1.0f, st);
+  }
+}
+
+int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64_t K,
+                             int64_t ld_in, const uint32_t* row_offsets,
+                             const uint32_t* scales_offsets, const int32_t* expert_ids,
+                             const float* sf, int32_t num_experts, const int32_t* row_indices,
+                             int32_t G, int64_t total_rows, int64_t total_scale_rows, void* out,
+                             void* scales, int32_t k_tiles_per_block, void* stream) {
+  if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
+  if (k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
+      k_tiles_per_block != 8)
+    return BSQ_ERR_VALUE;
+  if (G < 0 || G > (1 << 20)) return BSQ_ERR_VALUE;
+  if (in_rows < 0 || K < 0 || K % 32 != 0 || K >= (int64_t(1) << 31) || total_rows < 0 ||
+      total_scale_rows < 0 || total_scale_rows % 128 != 0 ||
+      total_scale_rows / 128 >= (int64_t(1) << 31))
+    return BSQ_ERR_SHAPE;
+  if (G == 0 || K == 0 || total_scale_rows == 0) return BSQ_OK;
+  if (ld_in < K) return BSQ_ERR_SHAPE;
+  if (!in || !row_offsets || !scales_offsets || !expert_ids || !out || !scales) return BSQ_ERR_NULL;
+  if (fmt == BSQ_NVFP4 && !sf) return BSQ_ERR_NULL;
+  if (fmt == BSQ_NVFP4 && num_experts < 1) return BSQ_ERR_VALUE;
+  if (!aligned(in, 16) || ld_in % 8 != 0 || !aligned(out, 16) || !aligned(scales, 16) ||
+      !aligned(row_offsets, 4) || !aligned(scales_offsets, 4) || !aligned(expert_ids, 4) ||
+      !aligned(sf, 4) || !aligned(row_indices, 4))
+    return BSQ_ERR_ALIGN;
+
+  GroupedArgs a;
+  a.in = static_cast<const uint16_t*>(in);
+  a.ld_in = ld_in;
+  a.in_rows = in_rows;
+  a.K = static_cast<int>(K);
+  a.row_offsets = row_offsets;
+  a.scales_offsets = scales_offsets;
+  a.expert_ids = expert_ids;
+  a.sf = sf;
+  a.num_experts = num_experts;
+  a.row_indices = row_indices;
+  a.G = G;
+  a.total_rows = total_rows;
+  a.total_scale_rows = total_scale_rows;
+  a.out = static_cast<uint8_t*>(out);
+  a.out_ld = row_bytes_of(fmt, K);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.kt_atoms = static_cast<int>(ceil_div(K, atom_cols_of(fmt)));
+  const int64_t tiles = total_scale_rows / 128;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (fmt) {
+    case BSQ_NVFP4: return launch_grouped<kNVFP4>(a, tiles, k_tiles_per_block, st);
+    case BSQ_MXFP4: return launch_grouped<kMXFP4>(a, tiles, k_tiles_per_block, st);
+    default: return launch_grouped<kMXFP8>(a, tiles, k_tiles_per_block, st);
+  }
+}
+
+int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_t ld,
+                              void* scales5d, void* stream) {
+  if (M < 0 || S < 0) return BSQ_ERR_SHAPE;
+  if (M == 0 || S == 0) return BSQ_OK;
+  if (ld < S) return BSQ_ERR_SHAPE;
+  const int64_t bands = ceil_div(M, 128), kt_atoms = ceil_div(S, 4);
+  const int64_t chunks = ceil_div(kt_atoms, kIlvAtoms);
+  if (bands >= (int64_t(1) << 31) || chunks > 65535 || kt_atoms >= (int64_t(1) << 31))
+    return BSQ_ERR_SHAPE;
+  if (!scales2d || !scales5d) return BSQ_ERR_NULL;
+  if (!aligned(scales5d, 16)) return BSQ_ERR_ALIGN;
+  const uint8_t* in = static_cast<const uint8_t*>(scales2d);
+  uint8_t* out = static_cast<uint8_t*>(scales5d);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dim3 grid(static_cast<unsigned>(bands), static_cast<unsigned>(chunks));
+  if (aligned(in, 4) && ld % 4 == 0 && S % 4 == 0)
+    interleave_kernel<true><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, static_cast<int>(kt_atoms));
+  else
+    interleave_kernel<false><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, static_cast<int>(kt_atoms));
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+int32_t bsq_device_error(void* stream, int32_t* code_out) {
+  if (!code_out) return BSQ_ERR_NULL;
+  *code_out = BSQ_OK;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BSQ_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return BSQ_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return BSQ_ERR_CUDA;
+  }
+  *code_out = static_cast<int32_t>(v);
+  return BSQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,231 @@
+// Dense block-scaled quantization: BF16 (M, K) -> packed NVFP4 / MXFP4 /
+// MXFP8 elements + scales in the 5D TCGEN layout.
+//
+// Design (sm_103a): a persistent kernel, one producer warp + four consumer
+// warps per CTA.  The work unit is a tile of 128 rows x 128 columns (one 5D
+// scale-tile row band, 2 atoms for NVFP4 / 1 atom for MX).  The producer's
+// elected lane streams tiles into a STAGES-deep shared-memory ring with 2D TMA
+// loads (two 128-row x 64-column boxes per tile, 128-byte swizzle,
+// out-of-range rows/columns zero-filled), completing on a "full" mbarrier.
+// Each consumer lane owns one row of the tile: it reads its row conflict-free
+// (the swizzle spreads a quarter-warp over all banks), reduces each block's
+// amax in registers, computes the block scale, encodes the elements with the
+// hardware cvt instructions and stores its packed bytes as whole 32-byte
+// sectors.  The lane -> row mapping is chosen so that the 32 lanes of a warp
+// hold 128 contiguous bytes of each 512-byte scale atom, written by one
+// coalesced 4-byte-per-lane store.  Consumer warps release a stage with one
+// arrive each on its "empty" mbarrier.  Zero-filled padding yields zero blocks,
+// whose scale bytes are 0x00, so the padding of the 5D buffer is written
+// without extra work.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace bsq {
+
+constexpr int kDenseTileRows = 128;
+constexpr int kDenseTileCols = 128;
+constexpr int kDenseBoxCols = 64;                               // 128 bytes of BF16
+constexpr int kDenseBoxBytes = kDenseTileRows * kDenseBoxCols * 2;  // 16 KB
+constexpr int kDenseStageBytes = 2 * kDenseBoxBytes;               // 32 KB
+constexpr int kDenseConsumerWarps = 4;
+constexpr int kDenseThreads = (kDenseConsumerWarps + 1) * 32;
+
+template <int STAGES>
+constexpr int dense_smem_bytes() {
+  return STAGES * kDenseStageBytes + 1024 /* alignment slack */ + 2 * STAGES * 8;
+}
+
+struct DenseArgs {
+  uint8_t* out;        // packed elements, row stride = packed row bytes
+  uint8_t* scales;     // 5D scales
+  int64_t out_ld;      // packed row bytes
+  int M, K;
+  int tiles_k;         // ceil(K / 128)
+  int num_tiles;       // ceil(M / 128) * tiles_k
+  int kt_atoms;        // 5D atoms per 128-row band: ceil(K / SF / 4)
+  int vec32;           // packed rows allow 32-byte stores
+  float tsf;
+};
+
+// Consumer work on one 64-column box of one row: returns the scale bytes of
+// the box's blocks (shifted into place by the caller) and stores the packed
+// elements.
+template <int FMT>
+__device__ __forceinline__ uint32_t dense_box_row(const uint8_t* box, int row, int64_t grow,
+                                                   int col0, const DenseArgs& a) {
+  // 8 x 16-byte chunks of this row; chunk c sits at c ^ (row % 8) (128B swizzle)
+  uint4 v[8];
+  const uint8_t* rp = box + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    v[c] = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
+
+  const bool full = col0 + kDenseBoxCols <= a.K;  // else exactly 32 valid columns
+  const bool row_ok = grow < a.M;
+  uint32_t scale_bytes = 0;
+
+  if constexpr (FMT == kNVFP4) {
+    uint32_t o[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t acc = 0;
+      acc = absmax2(acc, v[2 * b].x); acc = absmax2(acc, v[2 * b].y);
+      acc = absmax2(acc, v[2 * b].z); acc = absmax2(acc, v[2 * b].w);
+      acc = absmax2(acc, v[2 * b + 1].x); acc = absmax2(acc, v[2 * b + 1].y);
+      acc = absmax2(acc, v[2 * b + 1].z); acc = absmax2(acc, v[2 * b + 1].w);
+      const BlockScale sc = nvfp4_scale(absmax_final(acc), a.tsf);
+      o[2 * b] = quant8_e2m1(v[2 * b], sc.factor);
+      o[2 * b + 1] = quant8_e2m1(v[2 * b + 1], sc.factor);
+      scale_bytes |= sc.byte << (8 * b);
+    }
+    if (row_ok) {
+      uint8_t* dst = a.out + grow * a.out_ld + (col0 >> 1);
+      if (full && a.vec32) {
+        st_global_v8(dst, o);
+      } else {
+        st_global_v4(dst, o[0], o[1], o[2], o[3]);
+        if (full) st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
+      }
+    }
+  } else {
+    constexpr int QMAX = FMT == kMXFP4 ? 6 : 448;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int c = 4 * b; c < 4 * b + 4; ++c) {
+        acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
+        acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
+      }
+      const BlockScale sc = mx_scale<QMAX>(absmax_final(acc));
+      scale_bytes |= sc.byte << (8 * b);
+      if constexpr (FMT == kMXFP4) {
+        uint32_t o0 = quant8_e2m1(v[4 * b], sc.factor), o1 = quant8_e2m1(v[4 * b + 1], sc.factor);
+        uint32_t o2 = quant8_e2m1(v[4 * b + 2], sc.factor), o3 = quant8_e2m1(v[4 * b + 3], sc.factor);
+        if (row_ok && (b == 0 || full))
+          st_global_v4(a.out + grow * a.out_ld + ((col0 + 32 * b) >> 1), o0, o1, o2, o3);
+      } else {
+        uint32_t o[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint2 q = quant8_e4m3(v[4 * b + c], sc.factor);
+          o[2 * c] = q.x;
+          o[2 * c + 1] = q.y;
+        }
+        if (row_ok && (b == 0 || full)) {
+          uint8_t* dst = a.out + grow * a.out_ld + col0 + 32 * b;
+          if (a.vec32) {
+            st_global_v8(dst, o);
+          } else {
+            st_global_v4(dst, o[0], o[1], o[2], o[3]);
+            st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
+          }
+        }
+      }
+    }
+  }
+  return scale_bytes;
+}
+
+template <int FMT, int STAGES>
+__global__ void __launch_bounds__(kDenseThreads)
+    dense_quant_tma_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * kDenseStageBytes);
+  uint64_t* empty_bar = full_bar + STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kDenseConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kDenseConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmap);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_parity = 0;  // per-stage bit masks
+      for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u)) {
+          record_error(kErrTimeout);
+          break;
+        }
+        const int mt = t / a.tiles_k, kt = t - mt * a.tiles_k;
+        const int col0 = kt * kDenseTileCols;
+        const bool second = col0 + kDenseBoxCols < a.K;
+        uint8_t* dst = smem + stage * kDenseStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], second ? kDenseStageBytes : kDenseBoxBytes);
+        tma_load_2d(dst, &tmap, col0, mt * kDenseTileRows, &full_bar[stage]);
+        if (second)
+          tma_load_2d(dst + kDenseBoxBytes, &tmap, col0 + kDenseBoxCols, mt * kDenseTileRows,
+                      &full_bar[stage]);
+        used |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // Never leave the CTA with a TMA write still landing in shared memory.
+      for (int s = 0; s < STAGES; ++s)
+        if ((used >> s) & 1u)
+          if (!mbar_wait_bounded(&full_bar[s], (last_parity >> s) & 1u)) record_error(kErrTimeout);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // lane -> row: r32 = 8*warp + (lane % 8), r4 = lane / 8, row = r32 + 32*r4.
+  const int r32 = 8 * warp + (lane & 7);
+  const int r4 = lane >> 3;
+  const int row = r32 + 32 * r4;
+  const int atom_off = r32 * 16 + r4 * 4;  // this row's word inside a 512-byte atom
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    if (!mbar_wait_bounded(&full_bar[stage], phase)) {
+      record_error(kErrTimeout);
+      break;
+    }
+    const int mt = t / a.tiles_k, kt = t - mt * a.tiles_k;
+    const int col0 = kt * kDenseTileCols;
+    const int64_t grow = static_cast<int64_t>(mt) * kDenseTileRows + row;
+    const uint8_t* st = smem + stage * kDenseStageBytes;
+    uint8_t* band = a.scales + static_cast<int64_t>(mt) * a.kt_atoms * 512 + atom_off;
+
+    const uint32_t s0 = dense_box_row<FMT>(st, row, grow, col0, a);
+    const bool second = col0 + kDenseBoxCols < a.K;
+    uint32_t s1 = 0;
+    if (second) s1 = dense_box_row<FMT>(st + kDenseBoxBytes, row, grow, col0 + kDenseBoxCols, a);
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[stage]);
+
+    if constexpr (FMT == kNVFP4) {
+      // two atoms per tile (64 columns each)
+      *reinterpret_cast<uint32_t*>(band + (2 * kt) * 512) = s0;
+      if (second) *reinterpret_cast<uint32_t*>(band + (2 * kt + 1) * 512) = s1;
+    } else {
+      // one atom per tile: blocks 0,1 from box 0 and 2,3 from box 1
+      *reinterpret_cast<uint32_t*>(band + kt * 512) = s0 | (s1 << 16);
+    }
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+}  // namespace bsq

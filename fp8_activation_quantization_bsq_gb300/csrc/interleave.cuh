@@ -1,0 +1,59 @@
+// Rank-2 -> 5D TCGEN scale reinterleave (a pure byte permutation).
+//
+// Thread block (band, chunk) stages 128 rows x (4 * kIlvAtoms) scale bytes in
+// shared memory (zero outside M x S), then writes the chunk's atoms, which are
+// contiguous in the 5D buffer, as 16-byte stores: store j of an atom holds the
+// 4 bytes of rows j, j+32, j+64, j+96.  The staging rows are padded to 68
+// bytes so that the transposed 4-byte reads hit 32 distinct banks.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace bsq {
+
+constexpr int kIlvAtoms = 16;                 // atoms (4 scale columns each) per block
+constexpr int kIlvCols = 4 * kIlvAtoms;       // 64 scale bytes per row
+constexpr int kIlvPitch = kIlvCols + 4;       // padded staging row (bytes)
+constexpr int kIlvThreads = 128;
+
+template <bool WORDS>
+__global__ void __launch_bounds__(kIlvThreads)
+    interleave_kernel(const uint8_t* __restrict__ in, int64_t M, int64_t S, int64_t ld,
+                      uint8_t* __restrict__ out, int kt_atoms) {
+  __shared__ __align__(16) uint8_t tile[128 * kIlvPitch];
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int a0 = blockIdx.y * kIlvAtoms;
+  const int64_t s0 = static_cast<int64_t>(a0) * 4;
+
+  if constexpr (WORDS) {
+    // ld, S and the base are multiples of 4: one 4-byte word per thread step
+    for (int idx = threadIdx.x; idx < 128 * (kIlvCols / 4); idx += kIlvThreads) {
+      const int r = idx / (kIlvCols / 4), w = idx % (kIlvCols / 4);
+      const int64_t m = m0 + r, s = s0 + 4 * w;
+      uint32_t val = 0;
+      if (m < M && s < S) val = __ldg(reinterpret_cast<const uint32_t*>(in + m * ld + s));
+      *reinterpret_cast<uint32_t*>(tile + r * kIlvPitch + 4 * w) = val;
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < 128 * kIlvCols; idx += kIlvThreads) {
+      const int r = idx / kIlvCols, c = idx % kIlvCols;
+      const int64_t m = m0 + r, s = s0 + c;
+      tile[r * kIlvPitch + c] = (m < M && s < S) ? __ldg(in + m * ld + s) : uint8_t(0);
+    }
+  }
+  __syncthreads();
+
+  const int natoms = min(kIlvAtoms, kt_atoms - a0);
+  uint8_t* dst = out + (static_cast<int64_t>(blockIdx.x) * kt_atoms + a0) * 512;
+  for (int idx = threadIdx.x; idx < natoms * 32; idx += kIlvThreads) {
+    const int atom = idx >> 5, r32 = idx & 31;
+    const uint8_t* src = tile + r32 * kIlvPitch + atom * 4;
+    st_global_v4(dst + atom * 512 + r32 * 16,
+                 *reinterpret_cast<const uint32_t*>(src),
+                 *reinterpret_cast<const uint32_t*>(src + 32 * kIlvPitch),
+                 *reinterpret_cast<const uint32_t*>(src + 64 * kIlvPitch),
+                 *reinterpret_cast<const uint32_t*>(src + 96 * kIlvPitch));
+  }
+}
+
+}  // namespace bsq

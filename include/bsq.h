@@ -1,0 +1,186 @@
+/*
+ * bsq.h -- C ABI of libbsq: block-scaled quantization of BF16 activations to
+ * NVFP4, MXFP4 and MXFP8 with the scale factors written in the 5D TCGEN
+ * (tcgen05 block-scaled MMA) layout, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (Modular "block_scaled_quantization" pages):
+ *   - module index: "block-scaled quantization kernels for NVFP4, MXFP4, and
+ *     MXFP8"; block_scales_interleave "reinterleaves rank-2 scale factors into
+ *     the 5D TCGEN layout"; block_scaled_matmul_with_epilogue: callers
+ *     allocate the outputs;
+ *   - quantize_dynamic_scaled_async_fp4_kernel: per-group scale factors,
+ *     packed FP4 elements, FP32 tensor_sf, SF_VECTOR_SIZE;
+ *   - grouped_quantize_dynamic_scaled_fp4_async_kernel: per-expert tiles
+ *     located by a warp-parallel search over row_offsets / scales_offsets
+ *     (uint32), expert_ids (int32), per-expert FP32 sf_tensor, optional int32
+ *     row_indices, k_tiles_per_block column tiles per block.
+ *
+ * Formats and conventions (the pages name but do not define them; these are
+ * the readings this library implements bit-exactly):
+ *   NVFP4  E2M1 elements, one E4M3 scale per 16 elements.  Per block:
+ *          s = fl32(fl32(amax/6) * tensor_sf) -> E4M3 (nearest-even, satfinite);
+ *          os = (decoded scale == 0) ? 0 : fl32(tensor_sf / decoded scale);
+ *          q_i = E2M1(fl32(x_i * os)).
+ *   MXFP4  E2M1 elements, one E8M0 scale per 32; MXFP8 E4M3 elements, one E8M0
+ *          scale per 32.  Per block: s = fl32(amax/Qmax) (Qmax 6 / 448),
+ *          e = ceil(log2 s) clamped to [-127,127] (-127 when s == 0),
+ *          scale byte e+127, q_i = encode(fl32(x_i * 2^-e)).
+ *   Element encodes round to nearest, ties to the even code, saturate to the
+ *   largest finite magnitude and keep the sign bit (also of zero).
+ *   FP4 packing: element 2k in the low nibble of byte k.
+ *   Packed output: row-major, packed_row_bytes(fmt, K) bytes per row, rows
+ *   contiguous (no padding between rows).
+ *   5D scale layout, shape (ceil(rows/128), ceil(S/4), 32, 4, 4) bytes with
+ *   S = K/SF: the byte of (row m, scale column s) lives at
+ *     ((m/128)*Kt + s/4)*512 + (m%32)*16 + ((m%128)/32)*4 + (s%4),
+ *   Kt = ceil(S/4).
+ *   NaN or Inf inputs are outside the contract (results undefined).
+ *
+ * Ownership and execution: every pointer argument named *_dev is device
+ * memory allocated by the caller; the library allocates nothing and keeps no
+ * pointer after a call returns.  Compute calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream) of the calling thread's
+ * current CUDA device; they return after enqueueing.
+ *
+ * Errors: every function returns a bsq_status and never throws.  Arguments the
+ * host can check are checked before anything is enqueued (nothing is launched
+ * on error).  Device-resident metadata of the grouped call is bounds-checked
+ * on the device: an inconsistent entry skips the affected rows and records
+ * BSQ_ERR_VALUE in the per-device error word, readable with
+ * bsq_device_error().  Kernels that wait on asynchronous copies bound every
+ * wait (about one second); an expired wait records BSQ_ERR_TIMEOUT there.
+ */
+#ifndef BSQ_H
+#define BSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BSQ_API __attribute__((visibility("default")))
+#else
+#define BSQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSQ_NVFP4 = 0, /* E2M1 x16 + E4M3 scale + FP32 tensor_sf */
+  BSQ_MXFP4 = 1, /* E2M1 x32 + E8M0 scale */
+  BSQ_MXFP8 = 2  /* E4M3 x32 + E8M0 scale */
+} bsq_format;
+
+typedef enum {
+  BSQ_OK = 0,
+  BSQ_ERR_NULL = 1,    /* a required pointer is NULL */
+  BSQ_ERR_SHAPE = 2,   /* negative size, K not a multiple of 32, ld too small, ... */
+  BSQ_ERR_ALIGN = 3,   /* a pointer or row stride breaks the alignment stated below */
+  BSQ_ERR_VALUE = 4,   /* bad scalar (format, tensor_sf, k_tiles_per_block, G) or bad device metadata */
+  BSQ_ERR_CUDA = 5,    /* a CUDA runtime / driver call failed */
+  BSQ_ERR_TIMEOUT = 6  /* a bounded device-side wait expired */
+} bsq_status;
+
+/* Library version, (major << 16) | minor. */
+BSQ_API int32_t bsq_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+BSQ_API const char* bsq_status_string(int32_t status);
+
+/* Elements covered by one scale factor: 16 (NVFP4) or 32 (MXFP4 / MXFP8);
+ * 0 for an unknown format. */
+BSQ_API int32_t bsq_block_size(int32_t fmt);
+
+/* Bytes of one packed output row: K/2 for NVFP4 / MXFP4, K for MXFP8;
+ * 0 for an unknown format or K < 0. */
+BSQ_API int64_t bsq_packed_row_bytes(int32_t fmt, int64_t K);
+
+/* Bytes of a 5D scale buffer for `rows` rows of K elements:
+ * ceil(rows/128) * ceil(K/SF/4) * 512; 0 for bad arguments. */
+BSQ_API int64_t bsq_scales5d_bytes(int32_t fmt, int64_t rows, int64_t K);
+
+/*
+ * Dense quantize: an (M, K) BF16 matrix -> packed elements + 5D scales.
+ * (quantize_dynamic_scaled_fp4fp8 / quantize_dynamic_scaled_async_fp4_kernel)
+ *
+ *   fmt           bsq_format.
+ *   in_dev        BF16 input, row r at in_dev + r*ld_in elements; 16-byte aligned.
+ *   M, K          rows and columns; M >= 0, K >= 0, K % 32 == 0.  M == 0 or
+ *                 K == 0 is a no-op.  M < 2^31.
+ *   ld_in         input row stride in elements; ld_in >= K, ld_in % 8 == 0.
+ *   out_dev       packed output, M * bsq_packed_row_bytes(fmt, K) bytes;
+ *                 16-byte aligned.
+ *   scales5d_dev  bsq_scales5d_bytes(fmt, M, K) bytes; every byte is written
+ *                 (padding rows / columns of the last tiles get 0x00).
+ *   tensor_sf     NVFP4 per-tensor scale (finite, > 0); ignored for MX.
+ */
+BSQ_API int32_t bsq_quantize(int32_t fmt, const void* in_dev, int64_t M, int64_t K, int64_t ld_in,
+                     void* out_dev, void* scales5d_dev, float tensor_sf, void* stream);
+
+/*
+ * Grouped per-expert quantize (grouped_quantize_dynamic_scaled_fp4_async_kernel).
+ *
+ *   in_dev              BF16 source rows (in_rows x K, stride ld_in elements,
+ *                       16-byte aligned, ld_in % 8 == 0).
+ *   row_offsets_dev     uint32[G+1], non-decreasing, row_offsets[0] == 0:
+ *                       group g owns destination rows [row_offsets[g], row_offsets[g+1]).
+ *   scales_offsets_dev  uint32[G+1], non-decreasing multiples of 128,
+ *                       scales_offsets[0] == 0, scales_offsets[g+1]-scales_offsets[g]
+ *                       >= row count of g: first 5D scale row of group g.
+ *   expert_ids_dev      int32[G]: expert of group g; a negative id skips the group.
+ *   sf_dev              float[num_experts]: NVFP4 tensor_sf per expert
+ *                       (may be NULL for MX formats).
+ *   num_experts         length of sf_dev (>= 1 for NVFP4; ignored for MX).
+ *   row_indices_dev     int32[total_rows] or NULL: destination row d reads source
+ *                       row row_indices[d] (NULL: source row d).
+ *   G                   number of groups, 0 <= G <= 1<<20 (0 = no-op).
+ *   total_rows          destination rows allocated in out_dev; the device
+ *                       checks row_offsets[G] <= total_rows.
+ *   total_scale_rows    5D scale rows allocated (multiple of 128); the device
+ *                       checks scales_offsets[G] <= total_scale_rows.  The
+ *                       launch covers total_scale_rows/128 row tiles.
+ *   out_dev             total_rows * packed_row_bytes bytes: row d is written
+ *                       iff d belongs to a group with a non-negative expert id.
+ *   scales5d_dev        bsq_scales5d_bytes(fmt, total_scale_rows, K) bytes: each
+ *                       written row gets all ceil(S/4)*4 scale bytes (padding
+ *                       columns 0x00); padding rows are not written.
+ *   k_tiles_per_block   1, 2, 4 or 8 column tiles (64 columns for NVFP4, 128
+ *                       for MX) handled by one thread block.
+ * Device checks (error word BSQ_ERR_VALUE, the affected rows are skipped):
+ * a source row index outside [0, in_rows); row_offsets[G] > total_rows;
+ * scales_offsets[G] > total_scale_rows; scales_offsets[0] != 0; a group with
+ * more rows than its padded scale rows; an NVFP4 expert id >= num_experts.
+ */
+BSQ_API int32_t bsq_grouped_quantize(int32_t fmt, const void* in_dev, int64_t in_rows, int64_t K,
+                             int64_t ld_in, const uint32_t* row_offsets_dev,
+                             const uint32_t* scales_offsets_dev, const int32_t* expert_ids_dev,
+                             const float* sf_dev, int32_t num_experts,
+                             const int32_t* row_indices_dev, int32_t G,
+                             int64_t total_rows, int64_t total_scale_rows, void* out_dev,
+                             void* scales5d_dev, int32_t k_tiles_per_block, void* stream);
+
+/*
+ * Rank-2 -> 5D scale reinterleave (block_scales_interleave / _fp4 / _fp4_kernel).
+ *
+ *   scales2d_dev  M rows of S scale bytes, row stride ld bytes (ld >= S).
+ *   M, S          M >= 0, S >= 0 (either 0 = no-op).
+ *   scales5d_dev  ceil(M/128)*ceil(S/4)*512 bytes, all written (padding 0x00).
+ * A pure byte permutation: any 8-bit scale type (E4M3 or E8M0).
+ */
+BSQ_API int32_t bsq_scales_interleave(const void* scales2d_dev, int64_t M, int64_t S, int64_t ld,
+                              void* scales5d_dev, void* stream);
+
+/*
+ * Synchronize `stream`, then read and clear the current device's error word.
+ * *code_out receives BSQ_OK or the first device-side error recorded since the
+ * last call (BSQ_ERR_VALUE, BSQ_ERR_TIMEOUT).  Returns BSQ_ERR_CUDA if the
+ * synchronization itself fails (e.g. an earlier launch faulted).
+ */
+BSQ_API int32_t bsq_device_error(void* stream, int32_t* code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSQ_H */

@@ -1,0 +1,175 @@
+"""GPU parity of the grouped per-expert quantize against the CPU oracle, through
+the C ABI (Python binding): bit-exact packed rows and written scale bytes,
+sentinel canaries on everything the kernel must leave untouched (rows of
+skipped groups, padding scale rows, buffer margins), k_tiles_per_block in
+{1, 2, 4, 8}, with and without the row_indices gather, and device-side
+bounds checks that turn inconsistent metadata into BSQ_ERR_VALUE.
+
+Operation: grouped_quantize_dynamic_scaled_fp4_async_kernel (Modular
+block_scaled_quantization pages).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from bsq_testlib import SENTINEL, guarded, i32_device, margin_intact, to_device_bf16, u32_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    import fp8_activation_quantization_bsq_gb300 as m
+    from fp8_activation_quantization_bsq_gb300 import _build
+    _build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _run_grouped(bsq, fmt, d, kt, use_ridx=True, expert_ids=None, x_bits=None, ridx=None,
+                 expect_error=0):
+    x_bits = d["x_bits"] if x_bits is None else x_bits
+    K = x_bits.shape[1]
+    eid = d["expert_ids"] if expert_ids is None else expert_ids
+    ridx = (d["row_indices"] if use_ridx else None) if ridx is None else ridx
+    total_rows, tsr = d["total_rows"], d["total_scale_rows"]
+    ob = total_rows * oracle.packed_row_bytes(fmt, K)
+    sb = oracle.scales5d_bytes(tsr, K // oracle.block_size(fmt))
+    ofull, out = guarded(ob)
+    sfull, sc = guarded(sb)
+    bsq.grouped_quantize(to_device_bf16(x_bits), fmt, u32_device(d["row_offsets"]),
+                         u32_device(d["scales_offsets"]), i32_device(eid),
+                         torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
+                         i32_device(ridx) if ridx is not None else None,
+                         total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=kt,
+                         out=out, scales=sc)
+    assert bsq.device_error() == expect_error
+    assert margin_intact(ofull) and margin_intact(sfull)
+    return out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy()
+
+
+def _compare(fmt, d, p, s, use_ridx=True, expert_ids=None, x_bits=None, ridx=None):
+    x_bits = d["x_bits"] if x_bits is None else x_bits
+    eid = d["expert_ids"] if expert_ids is None else expert_ids
+    ridx = (d["row_indices"] if use_ridx else None) if ridx is None else ridx
+    p_ref, pw, s_ref, sw = oracle.grouped_quantize(fmt, x_bits, d["row_offsets"],
+                                                   d["scales_offsets"], eid, d["sf_tensor"], ridx)
+    np.testing.assert_array_equal(p[pw], p_ref[pw])
+    np.testing.assert_array_equal(s[sw], s_ref[sw])
+    assert np.all(p[~pw] == SENTINEL), "rows of skipped groups were written"
+    assert np.all(s[~sw] == SENTINEL), "padding scale rows were written"
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("kt", [1, 2, 4, 8])
+@pytest.mark.parametrize("K", [256, 96, 1120])
+def test_grouped_small(bsq, fmt, kt, K):
+    d = wl.config_grouped_prefill(seed=K + kt, tokens=96, K=K, num_experts=16, top_k=4, fmt=fmt)
+    p, s = _run_grouped(bsq, fmt, d, kt)
+    _compare(fmt, d, p, s)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+def test_grouped_identity_rows(bsq, fmt):
+    d = wl.config_grouped_prefill(seed=1, tokens=64, K=512, num_experts=8, top_k=2, fmt=fmt)
+    # without row_indices the destination row d reads source row d
+    x = wl.dense_activations(np.random.Generator(np.random.PCG64(2)), d["total_rows"], 512, "blocklognormal")
+    p, s = _run_grouped(bsq, fmt, d, 2, use_ridx=False, x_bits=x)
+    _compare(fmt, d, p, s, use_ridx=False, x_bits=x)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_grouped_large_groups_span_tiles(bsq, fmt):
+    # few experts, many rows each: groups span several 128-row tiles
+    d = wl.config_grouped_prefill(seed=9, tokens=600, K=320, num_experts=4, top_k=2, fmt=fmt)
+    assert max(np.diff(d["row_offsets"])) > 256
+    p, s = _run_grouped(bsq, fmt, d, 4)
+    _compare(fmt, d, p, s)
+
+
+def test_grouped_negative_expert_ids_are_skipped(bsq):
+    d = wl.config_grouped_prefill(seed=4, tokens=80, K=256, num_experts=16, top_k=4)
+    eid = d["expert_ids"].copy()
+    eid[::3] = -1
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, expert_ids=eid)
+    _compare("nvfp4", d, p, s, expert_ids=eid)
+
+
+def test_grouped_many_groups_search(bsq):
+    # G > 32 * 32 exercises more than two rounds of the warp-parallel search
+    d = wl.config_grouped_prefill(seed=6, tokens=2048, K=64, num_experts=1500, top_k=2, fmt="mxfp8")
+    assert d["G"] > 1024
+    p, s = _run_grouped(bsq, "mxfp8", d, 1)
+    _compare("mxfp8", d, p, s)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+@pytest.mark.parametrize("K", [7168, 2048])
+@pytest.mark.parametrize("kt", [1, 2, 4, 8])
+def test_grouped_decode_full_config(bsq, fmt, K, kt):
+    """Decode: 64 tokens, top-8 over 256 experts (512 rows, many 1-row
+    experts), row_indices gather -- fully compared."""
+    d = wl.config_grouped_decode(K=K, fmt=fmt)
+    assert d["total_rows"] / d["G"] <= 8
+    p, s = _run_grouped(bsq, fmt, d, kt)
+    _compare(fmt, d, p, s)
+
+
+def test_grouped_prefill_full_config_sampled(bsq):
+    """Prefill: 4096 tokens, top-8 over 256 experts, K=7168 (32768 rows) at
+    the benchmark's launch configuration; the oracle checks sampled groups
+    (the largest, the smallest and random ones)."""
+    d = wl.config_grouped_prefill()
+    kt = 8
+    p, s = _run_grouped(bsq, "nvfp4", d, kt)
+    m = np.diff(d["row_offsets"].astype(np.int64))
+    rng = np.random.Generator(np.random.PCG64(3))
+    groups = np.unique(np.concatenate([[np.argmax(m), np.argmin(m)], rng.choice(d["G"], 10, replace=False)]))
+    K = d["K"]
+    S = K // 16
+    Kt = -(-S // 4)
+    for gi in groups:
+        r0, r1 = int(d["row_offsets"][gi]), int(d["row_offsets"][gi + 1])
+        e = d["expert_ids"][gi]
+        pd, sd = oracle.quantize_rank2("nvfp4", d["x_bits"][d["row_indices"][r0:r1]], d["sf_tensor"][e])
+        np.testing.assert_array_equal(p[r0:r1], pd)
+        srow = int(d["scales_offsets"][gi]) + np.arange(r1 - r0)
+        mm, ss = np.meshgrid(srow, np.arange(S), indexing="ij")
+        np.testing.assert_array_equal(s[oracle.offset_5d(mm, ss, Kt)], sd)
+
+
+def test_grouped_bad_row_index_is_reported_not_faulted(bsq):
+    d = wl.config_grouped_prefill(seed=8, tokens=40, K=128, num_experts=8, top_k=2)
+    ridx = d["row_indices"].copy()
+    bad = [3, len(ridx) - 1]
+    ridx[bad[0]] = 10_000_000
+    ridx[bad[1]] = -5
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, ridx=ridx, expect_error=4)
+    p_ref, pw, _, _ = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"],
+                                              d["scales_offsets"], d["expert_ids"],
+                                              d["sf_tensor"], np.where(ridx < 0, 0, np.minimum(ridx, 39)))
+    good = np.ones(d["total_rows"], bool)
+    good[bad] = False
+    np.testing.assert_array_equal(p[good], p_ref[good])
+    assert np.all(p[bad] == SENTINEL)
+    # the error word is cleared by the read
+    assert bsq.device_error() == 0
+
+
+def test_grouped_offsets_beyond_buffers_are_reported(bsq):
+    """row_offsets[G] beyond total_rows: the overflowing group is skipped,
+    the error word says BSQ_ERR_VALUE and nothing lands past the buffers."""
+    d = wl.config_grouped_prefill(seed=8, tokens=40, K=128, num_experts=8, top_k=2)
+    d2 = dict(d)
+    d2["total_rows"] = d["total_rows"] - 1
+    p, s = _run_grouped(bsq, "nvfp4", d2, 1, expect_error=4)
+    last = d["G"] - 1
+    r0 = int(d["row_offsets"][last])
+    p_ref, _, _, _ = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"],
+                                             d["scales_offsets"], d["expert_ids"],
+                                             d["sf_tensor"], d["row_indices"])
+    np.testing.assert_array_equal(p[:r0], p_ref[:r0])
+    assert np.all(p[r0:] == SENTINEL)
