@@ -235,6 +235,8 @@ int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64
   a.out_ld = row_bytes_of(fmt, K);
   a.scales = static_cast<uint8_t*>(scales);
   a.kt_atoms = static_cast<int>(ceil_div(K, atom_cols_of(fmt)));
+  a.in_vec32 = aligned(in, 32) && ld_in % 16 == 0;
+  a.out_vec32 = aligned(out, 32) && a.out_ld % 32 == 0;
   const int64_t tiles = total_scale_rows / 128;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (fmt) {
@@ -259,10 +261,13 @@ int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_
   uint8_t* out = static_cast<uint8_t*>(scales5d);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   dim3 grid(static_cast<unsigned>(bands), static_cast<unsigned>(chunks));
-  if (aligned(in, 4) && ld % 4 == 0 && S % 4 == 0)
-    interleave_kernel<true><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, static_cast<int>(kt_atoms));
+  const int ikt = static_cast<int>(kt_atoms);
+  if (aligned(in, 16) && ld % 16 == 0 && S % 16 == 0)
+    interleave_kernel<16><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
+  else if (aligned(in, 4) && ld % 4 == 0 && S % 4 == 0)
+    interleave_kernel<4><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
   else
-    interleave_kernel<false><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, static_cast<int>(kt_atoms));
+    interleave_kernel<1><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 

@@ -1,13 +1,14 @@
 // Dense block-scaled quantization: BF16 (M, K) -> packed NVFP4 / MXFP4 /
 // MXFP8 elements + scales in the 5D TCGEN layout.
 //
-// Design (sm_103a): a persistent kernel, one producer warp + four consumer
+// Design (sm_103a): a persistent kernel, one producer warp + eight consumer
 // warps per CTA.  The work unit is a tile of 128 rows x 128 columns (one 5D
 // scale-tile row band, 2 atoms for NVFP4 / 1 atom for MX).  The producer's
 // elected lane streams tiles into a STAGES-deep shared-memory ring with 2D TMA
 // loads (two 128-row x 64-column boxes per tile, 128-byte swizzle,
 // out-of-range rows/columns zero-filled), completing on a "full" mbarrier.
-// Each consumer lane owns one row of the tile: it reads its row conflict-free
+// Consumer warps 0-3 take box 0 and warps 4-7 box 1 of every tile; each
+// consumer lane owns one row of its box: it reads its row conflict-free
 // (the swizzle spreads a quarter-warp over all banks), reduces each block's
 // amax in registers, computes the block scale, encodes the elements with the
 // hardware cvt instructions and stores its packed bytes as whole 32-byte
@@ -28,12 +29,13 @@ constexpr int kDenseTileCols = 128;
 constexpr int kDenseBoxCols = 64;                               // 128 bytes of BF16
 constexpr int kDenseBoxBytes = kDenseTileRows * kDenseBoxCols * 2;  // 16 KB
 constexpr int kDenseStageBytes = 2 * kDenseBoxBytes;               // 32 KB
-constexpr int kDenseConsumerWarps = 4;
+constexpr int kDenseConsumerWarps = 8;
 constexpr int kDenseThreads = (kDenseConsumerWarps + 1) * 32;
 
 template <int STAGES>
 constexpr int dense_smem_bytes() {
-  return STAGES * kDenseStageBytes + 1024 /* alignment slack */ + 2 * STAGES * 8;
+  // stages + alignment slack + mbarriers + NVFP4 element-scale and amax/6 tables
+  return STAGES * kDenseStageBytes + 1024 + 2 * STAGES * 8 + (256 + 128) * 4;
 }
 
 struct DenseArgs {
@@ -53,7 +55,9 @@ struct DenseArgs {
 // elements.
 template <int FMT>
 __device__ __forceinline__ uint32_t dense_box_row(const uint8_t* box, int row, int64_t grow,
-                                                   int col0, const DenseArgs& a) {
+                                                   int col0, const DenseArgs& a,
+                                                   const float* factor_tab,
+                                                   const float* div6_tab) {
   // 8 x 16-byte chunks of this row; chunk c sits at c ^ (row % 8) (128B swizzle)
   uint4 v[8];
   const uint8_t* rp = box + row * 128;
@@ -74,7 +78,7 @@ __device__ __forceinline__ uint32_t dense_box_row(const uint8_t* box, int row, i
       acc = absmax2(acc, v[2 * b].z); acc = absmax2(acc, v[2 * b].w);
       acc = absmax2(acc, v[2 * b + 1].x); acc = absmax2(acc, v[2 * b + 1].y);
       acc = absmax2(acc, v[2 * b + 1].z); acc = absmax2(acc, v[2 * b + 1].w);
-      const BlockScale sc = nvfp4_scale(absmax_final(acc), a.tsf);
+      const BlockScale sc = nvfp4_scale_tab(absmax_final(acc), a.tsf, factor_tab, div6_tab);
       o[2 * b] = quant8_e2m1(v[2 * b], sc.factor);
       o[2 * b + 1] = quant8_e2m1(v[2 * b + 1], sc.factor);
       scale_bytes |= sc.byte << (8 * b);
@@ -98,18 +102,18 @@ __device__ __forceinline__ uint32_t dense_box_row(const uint8_t* box, int row, i
         acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
         acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
       }
-      const BlockScale sc = mx_scale<QMAX>(absmax_final(acc));
+      const MxScale sc = mx_scale<QMAX>(absmax_final(acc));
       scale_bytes |= sc.byte << (8 * b);
       if constexpr (FMT == kMXFP4) {
-        uint32_t o0 = quant8_e2m1(v[4 * b], sc.factor), o1 = quant8_e2m1(v[4 * b + 1], sc.factor);
-        uint32_t o2 = quant8_e2m1(v[4 * b + 2], sc.factor), o3 = quant8_e2m1(v[4 * b + 3], sc.factor);
+        uint32_t o0 = quant8_e2m1_pow2(v[4 * b], sc.pow2), o1 = quant8_e2m1_pow2(v[4 * b + 1], sc.pow2);
+        uint32_t o2 = quant8_e2m1_pow2(v[4 * b + 2], sc.pow2), o3 = quant8_e2m1_pow2(v[4 * b + 3], sc.pow2);
         if (row_ok && (b == 0 || full))
           st_global_v4(a.out + grow * a.out_ld + ((col0 + 32 * b) >> 1), o0, o1, o2, o3);
       } else {
         uint32_t o[8];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint2 q = quant8_e4m3(v[4 * b + c], sc.factor);
+          const uint2 q = quant8_e4m3_pow2(v[4 * b + c], sc.pow2);
           o[2 * c] = q.x;
           o[2 * c + 1] = q.y;
         }
@@ -136,6 +140,8 @@ __global__ void __launch_bounds__(kDenseThreads)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * kDenseStageBytes);
   uint64_t* empty_bar = full_bar + STAGES;
+  float* factor_tab = reinterpret_cast<float*>(empty_bar + STAGES);
+  float* div6_tab = factor_tab + 256;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -146,6 +152,12 @@ __global__ void __launch_bounds__(kDenseThreads)
       mbar_init(&empty_bar[s], kDenseConsumerWarps);
     }
     fence_mbar_init();
+  }
+  if constexpr (FMT == kNVFP4) {
+    if (warp < kDenseConsumerWarps) {
+      fill_nvfp4_factor_table(factor_tab, a.tsf, threadIdx.x, 32 * kDenseConsumerWarps);
+      fill_div6_table(div6_tab, threadIdx.x, 32 * kDenseConsumerWarps);
+    }
   }
   __syncthreads();
 
@@ -186,8 +198,10 @@ __global__ void __launch_bounds__(kDenseThreads)
   }
 
   // -------------------------------------------------------------- consumers
-  // lane -> row: r32 = 8*warp + (lane % 8), r4 = lane / 8, row = r32 + 32*r4.
-  const int r32 = 8 * warp + (lane & 7);
+  // warp -> box h; lane -> row: r32 = 8*(warp%4) + lane%8, r4 = lane/8,
+  // row = r32 + 32*r4, so a warp's 32 scale words fill 128 contiguous bytes.
+  const int h = warp >> 2;
+  const int r32 = 8 * (warp & 3) + (lane & 7);
   const int r4 = lane >> 3;
   const int row = r32 + 32 * r4;
   const int atom_off = r32 * 16 + r4 * 4;  // this row's word inside a 512-byte atom
@@ -200,26 +214,23 @@ __global__ void __launch_bounds__(kDenseThreads)
       break;
     }
     const int mt = t / a.tiles_k, kt = t - mt * a.tiles_k;
-    const int col0 = kt * kDenseTileCols;
+    const int col0 = kt * kDenseTileCols + h * kDenseBoxCols;
+    const bool valid = col0 < a.K;
     const int64_t grow = static_cast<int64_t>(mt) * kDenseTileRows + row;
-    const uint8_t* st = smem + stage * kDenseStageBytes;
-    uint8_t* band = a.scales + static_cast<int64_t>(mt) * a.kt_atoms * 512 + atom_off;
-
-    const uint32_t s0 = dense_box_row<FMT>(st, row, grow, col0, a);
-    const bool second = col0 + kDenseBoxCols < a.K;
-    uint32_t s1 = 0;
-    if (second) s1 = dense_box_row<FMT>(st + kDenseBoxBytes, row, grow, col0 + kDenseBoxCols, a);
-
+    uint32_t sbytes = 0;
+    if (valid)
+      sbytes = dense_box_row<FMT>(smem + stage * kDenseStageBytes + h * kDenseBoxBytes, row, grow,
+                                  col0, a, factor_tab, div6_tab);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
 
+    uint8_t* band = a.scales + static_cast<int64_t>(mt) * a.kt_atoms * 512 + atom_off;
     if constexpr (FMT == kNVFP4) {
-      // two atoms per tile (64 columns each)
-      *reinterpret_cast<uint32_t*>(band + (2 * kt) * 512) = s0;
-      if (second) *reinterpret_cast<uint32_t*>(band + (2 * kt + 1) * 512) = s1;
+      // one atom (64 columns) per box
+      if (valid) *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
     } else {
-      // one atom per tile: blocks 0,1 from box 0 and 2,3 from box 1
-      *reinterpret_cast<uint32_t*>(band + kt * 512) = s0 | (s1 << 16);
+      // one atom per tile: box h holds its blocks 2h and 2h+1
+      *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = static_cast<uint16_t>(sbytes);
     }
     if (++stage == STAGES) {
       stage = 0;

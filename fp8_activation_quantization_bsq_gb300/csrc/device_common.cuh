@@ -33,15 +33,19 @@ __device__ __forceinline__ void record_error(unsigned code) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Running max of |x| over BF16 pairs; the result is two BF16 magnitudes.
+// Running max of |x| over BF16 pairs: max.xorsign.abs keeps max(|acc|, |w|)
+// per half (its sign bit is the XOR of the inputs' signs and is masked off at
+// the end).  NaN inputs are outside the contract.
 __device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
   uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7FFF7FFFu));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w));
   return r;
 }
 // Reduce the two halves of an absmax2 accumulator to one FP32 amax.  The
-// halves are non-negative BF16 values, which order like their bit patterns.
+// halves are BF16 magnitudes (after the sign mask), which order like their
+// bit patterns.
 __device__ __forceinline__ float absmax_final(uint32_t acc) {
+  acc &= 0x7FFF7FFFu;
   return __uint_as_float(max(acc << 16, acc & 0xFFFF0000u));
 }
 
@@ -59,57 +63,91 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-// Eight FP32 values -> eight E2M1 codes packed in one word, element 0 in the
-// low nibble.  cvt ...e2m1x2 puts its first source in the high nibble.
-__device__ __forceinline__ uint32_t pack_e2m1x8(float a0, float a1, float a2, float a3,
-                                                float a4, float a5, float a6, float a7) {
+// Scale the 8 BF16 elements of `w` by f (each product rounded to FP32, two
+// at a time with mul.rn.f32x2) and encode them as 8 E2M1 codes (one word,
+// element 0 in the low nibble).
+__device__ __forceinline__ uint32_t quant8_e2m1(uint4 w, float f) {
   uint32_t r;
-  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+  asm("{\n\t.reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .b64 p0, p1, p2, p3, ff;\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "shl.b32 l0, %1, 16;\n\tand.b32 h0, %1, 0xFFFF0000;\n\t"
+      "shl.b32 l1, %2, 16;\n\tand.b32 h1, %2, 0xFFFF0000;\n\t"
+      "shl.b32 l2, %3, 16;\n\tand.b32 h2, %3, 0xFFFF0000;\n\t"
+      "shl.b32 l3, %4, 16;\n\tand.b32 h3, %4, 0xFFFF0000;\n\t"
+      "mov.b64 ff, {%5, %5};\n\t"
+      "mov.b64 p0, {l0, h0};\n\tmul.rn.f32x2 p0, p0, ff;\n\tmov.b64 {l0, h0}, p0;\n\t"
+      "mov.b64 p1, {l1, h1};\n\tmul.rn.f32x2 p1, p1, ff;\n\tmov.b64 {l1, h1}, p1;\n\t"
+      "mov.b64 p2, {l2, h2};\n\tmul.rn.f32x2 p2, p2, ff;\n\tmov.b64 {l2, h2}, p2;\n\t"
+      "mov.b64 p3, {l3, h3};\n\tmul.rn.f32x2 p3, p3, ff;\n\tmov.b64 {l3, h3}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, h3, l3;\n\t"
       "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
       : "=r"(r)
-      : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "f"(f));
   return r;
 }
 
-// Four FP32 values -> four E4M3 bytes in one word, element 0 in the low byte.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+// Products of BF16 elements with a power of two p (given as BF16 bits, so p
+// is exact in BF16): fma.rn.f32.bf16(x, p, -0) is the exact product rounded
+// once to FP32, i.e. fl32(x * p), taking the BF16 halves of a word directly;
+// the -0 addend keeps the sign of zero products.
+#define BSQ_POW2_PRODUCTS_8                                                   \
+  ".reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, pw;\n\t"                         \
+  ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"                             \
+  "mov.b16 pw, %5;\n\t"                                                        \
+  "mov.b32 {x0, x1}, %1;\n\tmov.b32 {x2, x3}, %2;\n\t"                         \
+  "mov.b32 {x4, x5}, %3;\n\tmov.b32 {x6, x7}, %4;\n\t"                         \
+  "fma.rn.f32.bf16 y0, x0, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y1, x1, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y2, x2, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y3, x3, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y4, x4, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y5, x5, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y6, x6, pw, 0f80000000;\n\t"                                \
+  "fma.rn.f32.bf16 y7, x7, pw, 0f80000000;\n\t"
+
+// 8 BF16 elements x 2^k -> 8 E2M1 codes (one word, element 0 low).
+__device__ __forceinline__ uint32_t quant8_e2m1_pow2(uint4 w, uint16_t p_bf16) {
   uint32_t r;
-  asm("{\n\t.reg .b16 h0, h1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
-      "mov.b32 %0, {h0, h1};\n\t}"
+  asm("{\n\t" BSQ_POW2_PRODUCTS_8
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, y1, y0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, y3, y2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, y5, y4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, y7, y6;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
       : "=r"(r)
-      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "h"(p_bf16));
   return r;
 }
 
-// Scale the 8 BF16 elements of `w` by f (each product rounded to FP32) and
-// encode them as 8 E2M1 codes (one word).
-__device__ __forceinline__ uint32_t quant8_e2m1(uint4 w, float f) {
-  return pack_e2m1x8(__fmul_rn(bf16_lo(w.x), f), __fmul_rn(bf16_hi(w.x), f),
-                     __fmul_rn(bf16_lo(w.y), f), __fmul_rn(bf16_hi(w.y), f),
-                     __fmul_rn(bf16_lo(w.z), f), __fmul_rn(bf16_hi(w.z), f),
-                     __fmul_rn(bf16_lo(w.w), f), __fmul_rn(bf16_hi(w.w), f));
-}
-
-// Same for E4M3: 8 bytes (two words).
-__device__ __forceinline__ uint2 quant8_e4m3(uint4 w, float f) {
-  uint2 r;
-  r.x = pack_e4m3x4(__fmul_rn(bf16_lo(w.x), f), __fmul_rn(bf16_hi(w.x), f),
-                    __fmul_rn(bf16_lo(w.y), f), __fmul_rn(bf16_hi(w.y), f));
-  r.y = pack_e4m3x4(__fmul_rn(bf16_lo(w.z), f), __fmul_rn(bf16_hi(w.z), f),
-                    __fmul_rn(bf16_lo(w.w), f), __fmul_rn(bf16_hi(w.w), f));
-  return r;
+// 8 BF16 elements x 2^k -> 8 E4M3 bytes (two words, element 0 low).
+__device__ __forceinline__ uint2 quant8_e4m3_pow2(uint4 w, uint16_t p_bf16) {
+  uint64_t r;
+  asm("{\n\t" BSQ_POW2_PRODUCTS_8
+      ".reg .b16 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 q0, y1, y0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 q1, y3, y2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 q2, y5, y4;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 q3, y7, y6;\n\t"
+      "mov.b64 %0, {q0, q1, q2, q3};\n\t}"
+      : "=l"(r)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "h"(p_bf16));
+  return make_uint2(static_cast<uint32_t>(r), static_cast<uint32_t>(r >> 32));
 }
 
 // ----------------------------------------------------------- block scales --
 struct BlockScale {
   uint32_t byte;  // scale factor as stored (E4M3 or E8M0)
-  float factor;   // multiplier applied to the elements before encoding
+  float factor;   // NVFP4: FP32 multiplier applied to the elements before encoding
+};
+
+struct MxScale {
+  uint32_t byte;  // E8M0 scale byte e + 127
+  uint16_t pow2;  // 2^-e as BF16 bits (exact)
 };
 
 // NVFP4: s = fl32(fl32(amax / 6) * tensor_sf) -> E4M3; element scale
@@ -122,24 +160,60 @@ __device__ __forceinline__ BlockScale nvfp4_scale(float amax, float tsf) {
 }
 
 // MX: e = ceil(log2(fl32(amax / Qmax))) clamped to [-127, 127] (-127 for a
-// zero block), taken exactly from the FP32 bits of the quotient; byte e+127,
-// element factor 2^-e.
+// zero block); byte e+127, element factor 2^-e.
+//
+// No division is needed.  amax is a BF16 magnitude (8 significant bits) and
+// Qmax = 1.5 * 2^2 (E2M1) or 1.75 * 2^8 (E4M3).  The exact quotient r is a
+// power of two only when amax's significand equals Qmax's; otherwise r is at
+// least a relative 2^-9 away from every power of two, so rounding r to FP32
+// cannot reach one and ceil(log2(fl32(r))) = ceil(log2(r)).  With
+// amax = 1.f * 2^E: e = E - log2(Qmax / 1.q) + (1.f > 1.q), where 1.q is
+// Qmax's significand.  Zero and subnormal amax give e < -127 (clamped).
 template <int QMAX>
-__device__ __forceinline__ BlockScale mx_scale(float amax) {
-  const float s = __fdiv_rn(amax, static_cast<float>(QMAX));
-  const uint32_t bits = __float_as_uint(s);
-  const int ex = static_cast<int>(bits >> 23);
-  int e;
-  if (ex == 0) {
-    // zero or subnormal: s <= 2^-127 -> -127 (after the clamp), else -126
-    e = bits > 0x00400000u ? -126 : -127;
-  } else {
-    e = ex - 127 + ((bits & 0x007FFFFFu) != 0u ? 1 : 0);
-    e = min(e, 127);
+__device__ __forceinline__ MxScale mx_scale(float amax) {
+  static_assert(QMAX == 6 || QMAX == 448, "Qmax is 6 (E2M1) or 448 (E4M3)");
+  constexpr int kExpQ = QMAX == 6 ? 2 : 8;                        // Qmax = 1.q * 2^kExpQ
+  constexpr uint32_t kSigQ = QMAX == 6 ? 0x00400000u : 0x00600000u;  // 1.q fraction bits
+  const uint32_t bits = __float_as_uint(amax);
+  int e = static_cast<int>(bits >> 23) - 127 - kExpQ + ((bits & 0x007FFFFFu) > kSigQ ? 1 : 0);
+  e = max(e, -127);
+  // 2^-e is a normal BF16 value for e in [-127, 126], the range reachable here
+  return {static_cast<uint32_t>(e + 127), static_cast<uint16_t>((127 - e) << 7)};
+}
+
+// NVFP4 element-scale table: os[b] = tensor_sf / decode(b) for every E4M3
+// byte b (0 when the decoded value is 0; NaN codes are never produced by the
+// block-scale encode).  Filled once per thread block in shared memory so that
+// each block scale costs one lookup instead of a division.
+__device__ __forceinline__ void fill_nvfp4_factor_table(float* tab, float tsf, int tid, int nthreads) {
+  for (int b = tid; b < 256; b += nthreads) {
+    const float ds = e4m3_to_f32(static_cast<uint32_t>(b));
+    tab[b] = (ds == 0.0f || b == 0x7F || b == 0xFF) ? 0.0f : __fdiv_rn(tsf, fabsf(ds));
   }
-  // 2^-e: normal for -e >= -126; 2^-127 is the subnormal 0x00400000
-  const uint32_t fbits = (e == 127) ? 0x00400000u : static_cast<uint32_t>(127 - e) << 23;
-  return {static_cast<uint32_t>(e + 127), __uint_as_float(fbits)};
+}
+
+// fl32(amax / 6) without a division for BF16 amax.  With
+// amax = (1 + f/128) * 2^(E-127) (E the biased exponent, f the 7 fraction
+// bits), amax / 6 = ((128 + f) / 192) * 2^(E-129): the quotient of the
+// significands, rounded once, scaled by a power of two.  Scaling is exact
+// while the result stays normal (E >= 5); smaller amax take the division.
+// div6_tab[f] = fl32((128 + f) / 192).
+__device__ __forceinline__ void fill_div6_table(float* tab, int tid, int nthreads) {
+  for (int f = tid; f < 128; f += nthreads) tab[f] = __fdiv_rn(static_cast<float>(128 + f), 192.0f);
+}
+__device__ __forceinline__ float amax_div6(float amax, const float* div6_tab) {
+  const uint32_t bits = __float_as_uint(amax);
+  const uint32_t e = bits >> 23;
+  if (e < 5u) return __fdiv_rn(amax, 6.0f);
+  return __fmul_rn(div6_tab[(bits >> 16) & 0x7Fu], __uint_as_float((e - 2u) << 23));
+}
+
+// NVFP4 block scale via the tables: s = fl32(fl32(amax / 6) * tensor_sf) -> E4M3,
+// element factor factor_tab[byte].
+__device__ __forceinline__ BlockScale nvfp4_scale_tab(float amax, float tsf, const float* factor_tab,
+                                                      const float* div6_tab) {
+  const uint32_t b = f32_to_e4m3(__fmul_rn(amax_div6(amax, div6_tab), tsf));
+  return {b, factor_tab[b]};
 }
 
 // ------------------------------------------------------------------- PTX --
@@ -222,6 +296,14 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+// Read-only 32-byte global load that does not allocate in L1.
+__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(p));
 }
 
 // Read-only 16-byte global load that does not allocate in L1.

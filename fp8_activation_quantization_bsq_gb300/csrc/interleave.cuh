@@ -16,7 +16,9 @@ constexpr int kIlvCols = 4 * kIlvAtoms;       // 64 scale bytes per row
 constexpr int kIlvPitch = kIlvCols + 4;       // padded staging row (bytes)
 constexpr int kIlvThreads = 128;
 
-template <bool WORDS>
+// VEC: bytes per staging load (16, 4 or 1); the launcher picks the widest one
+// that the base address, ld and S allow.
+template <int VEC>
 __global__ void __launch_bounds__(kIlvThreads)
     interleave_kernel(const uint8_t* __restrict__ in, int64_t M, int64_t S, int64_t ld,
                       uint8_t* __restrict__ out, int kt_atoms) {
@@ -25,20 +27,49 @@ __global__ void __launch_bounds__(kIlvThreads)
   const int a0 = blockIdx.y * kIlvAtoms;
   const int64_t s0 = static_cast<int64_t>(a0) * 4;
 
-  if constexpr (WORDS) {
-    // ld, S and the base are multiples of 4: one 4-byte word per thread step
-    for (int idx = threadIdx.x; idx < 128 * (kIlvCols / 4); idx += kIlvThreads) {
-      const int r = idx / (kIlvCols / 4), w = idx % (kIlvCols / 4);
-      const int64_t m = m0 + r, s = s0 + 4 * w;
-      uint32_t val = 0;
-      if (m < M && s < S) val = __ldg(reinterpret_cast<const uint32_t*>(in + m * ld + s));
-      *reinterpret_cast<uint32_t*>(tile + r * kIlvPitch + 4 * w) = val;
+  if constexpr (VEC > 1) {
+    // every load of the thread is issued before the first shared-memory store
+    constexpr int kPerRow = kIlvCols / VEC;
+    constexpr int kN = 128 * kPerRow / kIlvThreads;
+    uint32_t val[kN][VEC / 4];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) {
+      const int idx = threadIdx.x + j * kIlvThreads;
+      const int r = idx / kPerRow, w = idx % kPerRow;
+      const int64_t m = m0 + r, s = s0 + VEC * w;
+      const bool in_range = m < M && s < S;
+      if constexpr (VEC == 16) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (in_range) x = __ldg(reinterpret_cast<const uint4*>(in + m * ld + s));
+        val[j][0] = x.x; val[j][1] = x.y; val[j][2] = x.z; val[j][3] = x.w;
+      } else {
+        val[j][0] = in_range ? __ldg(reinterpret_cast<const uint32_t*>(in + m * ld + s)) : 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kN; ++j) {
+      const int idx = threadIdx.x + j * kIlvThreads;
+      const int r = idx / kPerRow, w = idx % kPerRow;
+#pragma unroll
+      for (int k = 0; k < VEC / 4; ++k)
+        *reinterpret_cast<uint32_t*>(tile + r * kIlvPitch + VEC * w + 4 * k) = val[j][k];
     }
   } else {
-    for (int idx = threadIdx.x; idx < 128 * kIlvCols; idx += kIlvThreads) {
-      const int r = idx / kIlvCols, c = idx % kIlvCols;
-      const int64_t m = m0 + r, s = s0 + c;
-      tile[r * kIlvPitch + c] = (m < M && s < S) ? __ldg(in + m * ld + s) : uint8_t(0);
+    constexpr int kB = 16;
+    for (int base = 0; base < 128 * kIlvCols; base += kB * kIlvThreads) {
+      uint8_t val[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int idx = base + threadIdx.x + j * kIlvThreads;
+        const int r = idx / kIlvCols, c = idx % kIlvCols;
+        const int64_t m = m0 + r, s = s0 + c;
+        val[j] = (m < M && s < S) ? __ldg(in + m * ld + s) : uint8_t(0);
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int idx = base + threadIdx.x + j * kIlvThreads;
+        tile[(idx / kIlvCols) * kIlvPitch + idx % kIlvCols] = val[j];
+      }
     }
   }
   __syncthreads();

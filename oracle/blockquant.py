@@ -34,7 +34,8 @@ def _bf16_to_f32(x_bits: np.ndarray) -> np.ndarray:
 
 def nvfp4_block_scale(amax: np.ndarray, tsf: np.float32) -> np.ndarray:
     """NVFP4 block scale byte: E4M3(fl32(fl32(amax / 6) * tensor_sf))."""
-    s = (np.asarray(amax, np.float32) / np.float32(6.0)) * np.float32(tsf)
+    with np.errstate(over="ignore"):                 # +inf saturates to 448
+        s = (np.asarray(amax, np.float32) / np.float32(6.0)) * np.float32(tsf)
     return e4m3_encode(s)
 
 
@@ -71,7 +72,8 @@ def quantize_rank2(fmt: str, x_bits: np.ndarray, tensor_sf=1.0):
         tsf = np.float32(tensor_sf)
         scale_bytes = nvfp4_block_scale(amax, tsf)
         factor = nvfp4_element_scale(scale_bytes, tsf)
-        codes = e2m1_encode(blocks * factor[..., None])
+        with np.errstate(over="ignore"):             # +-inf saturates to +-6
+            codes = e2m1_encode(blocks * factor[..., None])
     else:
         e = mx_block_exponent(amax, 6.0 if fmt == "mxfp4" else 448.0)
         scale_bytes = (e + 127).astype(np.uint8)

@@ -195,3 +195,31 @@ def test_interleave_of_quantize_scales(bsq):
     _, s5_gpu = _run_dense(bsq, "nvfp4", c["x_bits"], c["tensor_sf"])
     out = bsq.scales_interleave(torch.from_numpy(s2).cuda())
     np.testing.assert_array_equal(out.cpu().numpy(), s5_gpu)
+
+
+def _amax_sweep_matrix(SF: int, per_row_blocks: int = 64):
+    """One block per positive finite BF16 value v (and one zero block):
+    elements v, -v, v/3, -v/7 (rounded to BF16) and zeros, so the block amax
+    runs over every BF16 magnitude."""
+    v = np.arange(0, 0x7F80, dtype=np.uint32).astype(np.uint16)          # +0 .. largest finite
+    vf = wl.bf16_bits_to_f32(v)
+    n = v.size
+    rows = -(-n // per_row_blocks)
+    blocks = np.zeros((rows * per_row_blocks, SF), np.uint16)
+    blocks[:n, 0] = v
+    blocks[:n, 1] = v | 0x8000
+    blocks[:n, 2] = wl.f32_to_bf16_bits(vf / np.float32(3.0))
+    blocks[:n, 3] = wl.f32_to_bf16_bits(vf / np.float32(-7.0))
+    return blocks.reshape(rows, per_row_blocks * SF)
+
+
+@pytest.mark.parametrize("fmt,tsf", [("mxfp4", 1.0), ("mxfp8", 1.0), ("nvfp4", 1.0),
+                                     ("nvfp4", 0.6640316), ("nvfp4", 1e-20), ("nvfp4", 1e20),
+                                     ("nvfp4", 2688.0)])
+def test_block_scale_exhaustive_amax(bsq, fmt, tsf):
+    """Every BF16 block amax -> scale byte and element codes, bit-exact."""
+    mat = _amax_sweep_matrix(oracle.block_size(fmt))
+    p, s = _run_dense(bsq, fmt, mat, np.float32(tsf))
+    p_ref, s_ref = oracle.quantize(fmt, mat, np.float32(tsf))
+    np.testing.assert_array_equal(s, s_ref)
+    np.testing.assert_array_equal(p, p_ref)

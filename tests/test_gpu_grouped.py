@@ -99,11 +99,20 @@ def test_grouped_negative_expert_ids_are_skipped(bsq):
 
 
 def test_grouped_many_groups_search(bsq):
-    # G > 32 * 32 exercises more than two rounds of the warp-parallel search
-    d = wl.config_grouped_prefill(seed=6, tokens=2048, K=64, num_experts=1500, top_k=2, fmt="mxfp8")
-    assert d["G"] > 1024
-    p, s = _run_grouped(bsq, "mxfp8", d, 1)
-    _compare("mxfp8", d, p, s)
+    """G = 3000 one- to three-row groups: more than two rounds of the
+    warp-parallel search over scales_offsets."""
+    rng = np.random.Generator(np.random.PCG64(6))
+    G = 3000
+    m = rng.integers(1, 4, size=G)
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = (np.arange(G + 1) * 128).astype(np.uint32)
+    x = wl.dense_activations(rng, int(ro[-1]), 64, "blocklognormal")
+    d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=np.arange(G, dtype=np.int32),
+             sf_tensor=np.ones(G, np.float32), row_indices=rng.permutation(int(ro[-1])).astype(np.int32),
+             total_rows=int(ro[-1]), total_scale_rows=int(so[-1]), G=G)
+    for fmt in ("mxfp8", "nvfp4"):
+        p, s = _run_grouped(bsq, fmt, d, 1)
+        _compare(fmt, d, p, s)
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
