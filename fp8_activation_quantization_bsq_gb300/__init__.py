@@ -22,10 +22,11 @@ import torch
 
 from ._build import LIB_PATH
 
-__all__ = ["FORMATS", "lib", "BsqError", "block_size", "packed_row_bytes", "scales5d_bytes",
+__all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes", "scales5d_bytes",
            "quantize", "grouped_quantize", "scales_interleave", "device_error", "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
+GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2}
 
 _c_i32, _c_i64, _c_f32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -39,6 +40,9 @@ _SIGNATURES = {
     "bsq_grouped_quantize": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p,
                                       _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_p,
                                       _c_i32, _c_p]),
+    "bsq_grouped_quantize_kernel": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p,
+                                             _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64,
+                                             _c_p, _c_p, _c_i32, _c_i32, _c_p]),
     "bsq_scales_interleave": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
     "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),
 }
@@ -126,14 +130,16 @@ def quantize(x: torch.Tensor, fmt, tensor_sf: float = 1.0, out=None, scales=None
 def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_ids,
                      sf_tensor=None, row_indices=None, total_rows: int | None = None,
                      total_scale_rows: int | None = None, k_tiles_per_block: int = 1,
-                     out=None, scales=None, stream=None):
+                     out=None, scales=None, stream=None, kernel: str = "auto"):
     """Grouped per-expert quantize of the (in_rows, K) BF16 CUDA tensor ``x``.
 
     ``row_offsets`` / ``scales_offsets`` are uint32 (stored as torch.int32
     bit patterns or uint32) CUDA tensors of G+1 entries, ``expert_ids`` int32
     [G], ``sf_tensor`` float32 [num_experts] (NVFP4), ``row_indices`` int32 or
     None.  ``total_rows`` / ``total_scale_rows`` size the outputs (required
-    when ``out`` / ``scales`` are not given).
+    when ``out`` / ``scales`` are not given).  ``kernel``: "auto", "stream"
+    (groups of many rows) or "latency" (groups of a few rows); the results
+    do not depend on it.
     Returns (packed uint8 (total_rows, packed_row_bytes), scales uint8).
     """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
@@ -153,11 +159,11 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
         scales = torch.empty(scales5d_bytes(f, total_scale_rows, K), dtype=torch.uint8, device=x.device)
     num_experts = sf_tensor.numel() if sf_tensor is not None else 0
     with torch.cuda.device(x.device):
-        rc = lib().bsq_grouped_quantize(
+        rc = lib().bsq_grouped_quantize_kernel(
             f, _ptr(x), in_rows, K, x.stride(0) if in_rows else K, _ptr(row_offsets),
             _ptr(scales_offsets), _ptr(expert_ids), _ptr(sf_tensor), num_experts,
             _ptr(row_indices), G, total_rows, total_scale_rows, _ptr(out), _ptr(scales),
-            k_tiles_per_block, _stream(x.device, stream))
+            k_tiles_per_block, GROUPED_KERNELS[kernel], _stream(x.device, stream))
     _check(rc, "bsq_grouped_quantize")
     return out, scales
 

@@ -21,6 +21,11 @@ using namespace bsq;
 
 constexpr int kDenseStages = 3;
 constexpr int kMaxDevices = 64;
+// Grouped quantize: groups averaging at most kGroupedLatencyMaxAvgRows rows
+// (decode) take the row kernel (kRowsPerWarp destination rows per warp),
+// larger groups (prefill) the 128-row tile kernel.
+constexpr int64_t kGroupedLatencyMaxAvgRows = 16;
+constexpr int kRowsPerWarp = 2;
 
 struct DeviceInfo {
   bool ready = false;
@@ -123,21 +128,39 @@ bsq_status launch_dense(const void* in, int64_t M, int64_t K, int64_t ld_in, voi
 }
 
 template <int FMT, int KT>
-bsq_status launch_grouped_kt(const GroupedArgs& a, int64_t tiles, cudaStream_t stream) {
+bsq_status launch_grouped_rows(const GroupedArgs& a, cudaStream_t stream) {
   const int64_t chunks = ceil_div(a.kt_atoms, KT);
-  if (chunks > 65535) return BSQ_ERR_SHAPE;
-  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
-  grouped_quant_kernel<FMT, KT><<<grid, kGroupedThreads, 0, stream>>>(a);
+  const int64_t blocks = ceil_div(a.total_rows, static_cast<int64_t>(kGrWarps) * kRowsPerWarp);
+  if (chunks > 65535 || blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  if (blocks == 0) return BSQ_OK;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(chunks));
+  grouped_rows_kernel<FMT, KT, kRowsPerWarp><<<grid, kGrThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 template <int FMT>
-bsq_status launch_grouped(const GroupedArgs& a, int64_t tiles, int kt, cudaStream_t stream) {
+bsq_status launch_grouped_tiles(GroupedArgs a, int kt, cudaStream_t stream) {
+  a.tiles_k = static_cast<int>(ceil_div(a.K, 128));
+  const int per = kt * atom_cols_of(FMT) / 128;   // 128-column tiles per block
+  a.ktc = per > 0 ? per : 1;
+  const int64_t chunks = ceil_div(a.tiles_k, a.ktc);
+  const int64_t tiles = a.total_scale_rows / 128;
+  if (chunks > 65535 || tiles >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
+  grouped_tile_kernel<FMT><<<grid, kGtThreads, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+template <int FMT>
+bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t stream) {
+  if (kernel == BSQ_GROUPED_AUTO)
+    kernel = a.total_rows <= kGroupedLatencyMaxAvgRows * a.G ? BSQ_GROUPED_LATENCY : BSQ_GROUPED_STREAM;
+  if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_tiles<FMT>(a, kt, stream);
   switch (kt) {
-    case 1: return launch_grouped_kt<FMT, 1>(a, tiles, stream);
-    case 2: return launch_grouped_kt<FMT, 2>(a, tiles, stream);
-    case 4: return launch_grouped_kt<FMT, 4>(a, tiles, stream);
-    default: return launch_grouped_kt<FMT, 8>(a, tiles, stream);
+    case 1: return launch_grouped_rows<FMT, 1>(a, stream);
+    case 2: return launch_grouped_rows<FMT, 2>(a, stream);
+    case 4: return launch_grouped_rows<FMT, 4>(a, stream);
+    default: return launch_grouped_rows<FMT, 8>(a, stream);
   }
 }
 
@@ -192,15 +215,18 @@ int32_t bsq_quantize(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t 
   }
 }
 
-int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64_t K,
-                             int64_t ld_in, const uint32_t* row_offsets,
-                             const uint32_t* scales_offsets, const int32_t* expert_ids,
-                             const float* sf, int32_t num_experts, const int32_t* row_indices,
-                             int32_t G, int64_t total_rows, int64_t total_scale_rows, void* out,
-                             void* scales, int32_t k_tiles_per_block, void* stream) {
+int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows, int64_t K,
+                                    int64_t ld_in, const uint32_t* row_offsets,
+                                    const uint32_t* scales_offsets, const int32_t* expert_ids,
+                                    const float* sf, int32_t num_experts,
+                                    const int32_t* row_indices, int32_t G, int64_t total_rows,
+                                    int64_t total_scale_rows, void* out, void* scales,
+                                    int32_t k_tiles_per_block, int32_t kernel, void* stream) {
   if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
   if (k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
       k_tiles_per_block != 8)
+    return BSQ_ERR_VALUE;
+  if (kernel != BSQ_GROUPED_AUTO && kernel != BSQ_GROUPED_STREAM && kernel != BSQ_GROUPED_LATENCY)
     return BSQ_ERR_VALUE;
   if (G < 0 || G > (1 << 20)) return BSQ_ERR_VALUE;
   if (in_rows < 0 || K < 0 || K % 32 != 0 || K >= (int64_t(1) << 31) || total_rows < 0 ||
@@ -217,7 +243,7 @@ int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64
       !aligned(sf, 4) || !aligned(row_indices, 4))
     return BSQ_ERR_ALIGN;
 
-  GroupedArgs a;
+  GroupedArgs a{};
   a.in = static_cast<const uint16_t*>(in);
   a.ld_in = ld_in;
   a.in_rows = in_rows;
@@ -225,7 +251,7 @@ int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64
   a.row_offsets = row_offsets;
   a.scales_offsets = scales_offsets;
   a.expert_ids = expert_ids;
-  a.sf = sf;
+  a.sf = fmt == BSQ_NVFP4 ? sf : nullptr;
   a.num_experts = num_experts;
   a.row_indices = row_indices;
   a.G = G;
@@ -237,13 +263,24 @@ int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64
   a.kt_atoms = static_cast<int>(ceil_div(K, atom_cols_of(fmt)));
   a.in_vec32 = aligned(in, 32) && ld_in % 16 == 0;
   a.out_vec32 = aligned(out, 32) && a.out_ld % 32 == 0;
-  const int64_t tiles = total_scale_rows / 128;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (fmt) {
-    case BSQ_NVFP4: return launch_grouped<kNVFP4>(a, tiles, k_tiles_per_block, st);
-    case BSQ_MXFP4: return launch_grouped<kMXFP4>(a, tiles, k_tiles_per_block, st);
-    default: return launch_grouped<kMXFP8>(a, tiles, k_tiles_per_block, st);
+    case BSQ_NVFP4: return launch_grouped<kNVFP4>(a, k_tiles_per_block, kernel, st);
+    case BSQ_MXFP4: return launch_grouped<kMXFP4>(a, k_tiles_per_block, kernel, st);
+    default: return launch_grouped<kMXFP8>(a, k_tiles_per_block, kernel, st);
   }
+}
+
+int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64_t K,
+                             int64_t ld_in, const uint32_t* row_offsets,
+                             const uint32_t* scales_offsets, const int32_t* expert_ids,
+                             const float* sf, int32_t num_experts, const int32_t* row_indices,
+                             int32_t G, int64_t total_rows, int64_t total_scale_rows, void* out,
+                             void* scales, int32_t k_tiles_per_block, void* stream) {
+  return bsq_grouped_quantize_kernel(fmt, in, in_rows, K, ld_in, row_offsets, scales_offsets,
+                                     expert_ids, sf, num_experts, row_indices, G, total_rows,
+                                     total_scale_rows, out, scales, k_tiles_per_block,
+                                     BSQ_GROUPED_AUTO, stream);
 }
 
 int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_t ld,

@@ -20,6 +20,7 @@
 // without extra work.
 #pragma once
 
+#include "box_quant.cuh"
 #include "device_common.cuh"
 
 namespace bsq {
@@ -50,88 +51,6 @@ struct DenseArgs {
   float tsf;
 };
 
-// Consumer work on one 64-column box of one row: returns the scale bytes of
-// the box's blocks (shifted into place by the caller) and stores the packed
-// elements.
-template <int FMT>
-__device__ __forceinline__ uint32_t dense_box_row(const uint8_t* box, int row, int64_t grow,
-                                                   int col0, const DenseArgs& a,
-                                                   const float* factor_tab,
-                                                   const float* div6_tab) {
-  // 8 x 16-byte chunks of this row; chunk c sits at c ^ (row % 8) (128B swizzle)
-  uint4 v[8];
-  const uint8_t* rp = box + row * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    v[c] = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
-
-  const bool full = col0 + kDenseBoxCols <= a.K;  // else exactly 32 valid columns
-  const bool row_ok = grow < a.M;
-  uint32_t scale_bytes = 0;
-
-  if constexpr (FMT == kNVFP4) {
-    uint32_t o[8];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      uint32_t acc = 0;
-      acc = absmax2(acc, v[2 * b].x); acc = absmax2(acc, v[2 * b].y);
-      acc = absmax2(acc, v[2 * b].z); acc = absmax2(acc, v[2 * b].w);
-      acc = absmax2(acc, v[2 * b + 1].x); acc = absmax2(acc, v[2 * b + 1].y);
-      acc = absmax2(acc, v[2 * b + 1].z); acc = absmax2(acc, v[2 * b + 1].w);
-      const BlockScale sc = nvfp4_scale_tab(absmax_final(acc), a.tsf, factor_tab, div6_tab);
-      o[2 * b] = quant8_e2m1(v[2 * b], sc.factor);
-      o[2 * b + 1] = quant8_e2m1(v[2 * b + 1], sc.factor);
-      scale_bytes |= sc.byte << (8 * b);
-    }
-    if (row_ok) {
-      uint8_t* dst = a.out + grow * a.out_ld + (col0 >> 1);
-      if (full && a.vec32) {
-        st_global_v8(dst, o);
-      } else {
-        st_global_v4(dst, o[0], o[1], o[2], o[3]);
-        if (full) st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
-      }
-    }
-  } else {
-    constexpr int QMAX = FMT == kMXFP4 ? 6 : 448;
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      uint32_t acc = 0;
-#pragma unroll
-      for (int c = 4 * b; c < 4 * b + 4; ++c) {
-        acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
-        acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
-      }
-      const MxScale sc = mx_scale<QMAX>(absmax_final(acc));
-      scale_bytes |= sc.byte << (8 * b);
-      if constexpr (FMT == kMXFP4) {
-        uint32_t o0 = quant8_e2m1_pow2(v[4 * b], sc.pow2), o1 = quant8_e2m1_pow2(v[4 * b + 1], sc.pow2);
-        uint32_t o2 = quant8_e2m1_pow2(v[4 * b + 2], sc.pow2), o3 = quant8_e2m1_pow2(v[4 * b + 3], sc.pow2);
-        if (row_ok && (b == 0 || full))
-          st_global_v4(a.out + grow * a.out_ld + ((col0 + 32 * b) >> 1), o0, o1, o2, o3);
-      } else {
-        uint32_t o[8];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint2 q = quant8_e4m3_pow2(v[4 * b + c], sc.pow2);
-          o[2 * c] = q.x;
-          o[2 * c + 1] = q.y;
-        }
-        if (row_ok && (b == 0 || full)) {
-          uint8_t* dst = a.out + grow * a.out_ld + col0 + 32 * b;
-          if (a.vec32) {
-            st_global_v8(dst, o);
-          } else {
-            st_global_v4(dst, o[0], o[1], o[2], o[3]);
-            st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
-          }
-        }
-      }
-    }
-  }
-  return scale_bytes;
-}
-
 template <int FMT, int STAGES>
 __global__ void __launch_bounds__(kDenseThreads)
     dense_quant_tma_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
@@ -153,13 +72,7 @@ __global__ void __launch_bounds__(kDenseThreads)
     }
     fence_mbar_init();
   }
-  if constexpr (FMT == kNVFP4) {
-    if (warp < kDenseConsumerWarps) {
-      fill_nvfp4_factor_table(factor_tab, a.tsf, threadIdx.x, 32 * kDenseConsumerWarps);
-      fill_div6_table(div6_tab, threadIdx.x, 32 * kDenseConsumerWarps);
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // barriers ready: the producer starts streaming at once
 
   if (warp == kDenseConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -198,6 +111,14 @@ __global__ void __launch_bounds__(kDenseThreads)
   }
 
   // -------------------------------------------------------------- consumers
+  // NVFP4 scale tables, filled while the first tiles are in flight; named
+  // barrier 1 synchronizes the consumer warps only.
+  if constexpr (FMT == kNVFP4) {
+    fill_nvfp4_factor_table(factor_tab, a.tsf, threadIdx.x, 32 * kDenseConsumerWarps);
+    fill_div6_table(div6_tab, threadIdx.x, 32 * kDenseConsumerWarps);
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kDenseConsumerWarps) : "memory");
+  }
+
   // warp -> box h; lane -> row: r32 = 8*(warp%4) + lane%8, r4 = lane/8,
   // row = r32 + 32*r4, so a warp's 32 scale words fill 128 contiguous bytes.
   const int h = warp >> 2;
@@ -205,6 +126,7 @@ __global__ void __launch_bounds__(kDenseThreads)
   const int r4 = lane >> 3;
   const int row = r32 + 32 * r4;
   const int atom_off = r32 * 16 + r4 * 4;  // this row's word inside a 512-byte atom
+  const NvScale ns{a.tsf, factor_tab, nullptr, div6_tab};
 
   int stage = 0;
   uint32_t phase = 0;
@@ -218,9 +140,13 @@ __global__ void __launch_bounds__(kDenseThreads)
     const bool valid = col0 < a.K;
     const int64_t grow = static_cast<int64_t>(mt) * kDenseTileRows + row;
     uint32_t sbytes = 0;
-    if (valid)
-      sbytes = dense_box_row<FMT>(smem + stage * kDenseStageBytes + h * kDenseBoxBytes, row, grow,
-                                  col0, a, factor_tab, div6_tab);
+    if (valid) {
+      uint8_t* dst = grow < a.M ? a.out + grow * a.out_ld +
+                                      (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0)
+                                : nullptr;
+      sbytes = quant_box_row<FMT, true>(smem + stage * kDenseStageBytes + h * kDenseBoxBytes + row * 128,
+                                        row, min(kDenseBoxCols, a.K - col0), dst, a.vec32 != 0, ns);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
 

@@ -1,31 +1,40 @@
 // Grouped per-expert block-scaled quantization (MoE activations).
 //
-// The 5D scale buffer is cut into 128-row tiles; the groups' scale rows are
-// padded to whole tiles (scales_offsets are multiples of 128), so every tile
-// belongs to exactly one group.  Thread block (tile, chunk) handles one tile
-// and KT consecutive 5D atom columns (k_tiles_per_block): warp 0 finds the
-// group with a warp-parallel search over scales_offsets (256 probes per
-// round, one round of loads for up to 256 groups, row_offsets / expert_ids
-// read in the same round) and broadcasts it through shared memory; batching KT column
-// tiles per block amortizes that search and shrinks the grid, which dominates
-// at decode where a tile holds a few routed rows.
+// Each destination row d belongs to the group g with row_offsets[g] <= d <
+// row_offsets[g+1]; its scales go to 5D row scales_offsets[g] + (d -
+// row_offsets[g]) (groups padded to whole 128-row tiles), its NVFP4 tensor
+// scale is sf_tensor[expert_ids[g]], and it reads source row row_indices[d]
+// (or d).  Two kernels, one per regime, give identical bytes:
 //
-// Work inside a block: one thread per scale block (16 or 32 elements of one
-// row), consecutive threads on consecutive blocks of a row, so a warp reads
-// and writes contiguous runs (256-bit loads of the gathered source row).
-// Each thread reduces its block's amax in registers, derives the scale
-// (NVFP4 through the division-free amax/6 and the per-block element-scale
-// table; MX from the exponent bits), encodes and stores its elements; the
-// four scale bytes of a row's atom are OR-reduced over 4 lanes and written as
-// one word.  Blocks of the last atom that lie beyond K are zero, giving scale
-// byte 0x00.
+//  * grouped_tile_kernel (groups of many rows, prefill).  A thread block owns
+//    one 128-row scale tile, which lies inside one group, and a run of
+//    128-column tiles (k_tiles_per_block atom columns): warp 0 finds the group
+//    with a warp-parallel search over scales_offsets (rounds of 256 probes;
+//    the last round also reads row_offsets and expert_ids at the probe
+//    positions, so up to 256 groups cost one round of loads).  Then, as in
+//    the dense kernel, each lane owns one row and one 64-column half of a
+//    tile, loads its gathered row segment with 256-bit loads (whole 32-byte
+//    sectors per lane), double-buffered across the column tiles, quantizes it
+//    in registers with the block's element-scale table and stores whole
+//    sectors; a warp's 32 scale words form one coalesced 128-byte store.
+//
+//  * grouped_rows_kernel (groups of a few rows, decode).  A warp owns R
+//    consecutive destination rows and one run of k_tiles_per_block atom
+//    columns, whatever the group sizes.  Lane r resolves row d0 + r by a
+//    binary search over row_offsets (L1-resident), then the rows' scale
+//    blocks are spread over the lanes, consecutive blocks on consecutive
+//    lanes, each lane quantizing whole blocks; the scale bytes of a row's
+//    atom are OR-reduced over 4 lanes into one word.
+//
+// Batching column tiles per unit (k_tiles_per_block) amortizes the lookups
+// and shrinks the grid, which dominates at decode where a unit carries a few
+// routed rows.  Blocks of the last atom beyond K are zero (scale 0x00).
 #pragma once
 
+#include "box_quant.cuh"
 #include "device_common.cuh"
 
 namespace bsq {
-
-constexpr int kGroupedThreads = 128;
 
 struct GroupedArgs {
   const uint16_t* in;
@@ -35,7 +44,7 @@ struct GroupedArgs {
   const uint32_t* row_offsets;
   const uint32_t* scales_offsets;
   const int32_t* expert_ids;
-  const float* sf;
+  const float* sf;      // null for MX formats
   int num_experts;
   const int32_t* row_indices;  // may be null
   int G;
@@ -47,10 +56,22 @@ struct GroupedArgs {
   int kt_atoms;         // atoms per 128-row band
   int in_vec32;         // input rows allow 32-byte loads
   int out_vec32;        // packed rows allow 32-byte stores
+  int tiles_k;          // 128-column tiles per row (tile kernel)
+  int ktc;              // 128-column tiles per thread block (tile kernel)
 };
 
-// Pick entry j (0..255, warp-uniform) of a 256-entry array held as 8
-// registers per lane (entry j in register j/32 of lane j%32).
+// Checks of the offsets' first and last entries (one thread reports).
+__device__ __forceinline__ void check_offsets(const GroupedArgs& a) {
+  if (__ldg(a.row_offsets) != 0u || __ldg(a.scales_offsets) != 0u ||
+      static_cast<int64_t>(__ldg(a.row_offsets + a.G)) > a.total_rows ||
+      static_cast<int64_t>(__ldg(a.scales_offsets + a.G)) > a.total_scale_rows)
+    record_error(kErrValue);
+}
+
+// ------------------------------------------------------ grouped_tile_kernel --
+
+// Entry j (0..255, warp-uniform) of a 256-entry array held as 8 registers
+// per lane (entry j in register j/32 of lane j%32).
 template <typename T>
 __device__ __forceinline__ T warp_pick(const T (&reg)[8], int j) {
   T v = reg[0];
@@ -60,33 +81,27 @@ __device__ __forceinline__ T warp_pick(const T (&reg)[8], int j) {
   return __shfl_sync(0xFFFFFFFFu, v, j & 31);
 }
 
-struct GroupHit {
-  int64_t so_g, so_n, r_beg, r_end;
-  int e;
+struct TileInfo {
+  int64_t dst0;   // destination row of the tile's first row
+  int n;          // rows of the tile to quantize (0: none)
+  int e;          // expert id
 };
 
-// Locate the group of padded scale row `row0`: g = max{g : so[g] <= row0}
-// for non-decreasing scales_offsets with so[0] <= row0 < so[G].  Runs on one
-// full warp.  Rounds of 256 evenly spaced probes (8 loads per lane, issued
-// together, counted with ballots) narrow the range 256-fold; the final round
-// (step 1) also loads row_offsets and expert_ids at the probe positions, so
-// the group's bounds and expert come out of registers by shuffles: for up to
-// 256 groups the whole search is one round of loads.
-__device__ __forceinline__ GroupHit warp_group_search(const GroupedArgs& a, int64_t row0) {
+// Resolve the 128-row scale tile starting at row0 (warp-collective):
+// g = max{g : so[g] <= row0}, then the tile's rows in group g.  Inconsistent
+// metadata records BSQ_ERR_VALUE and leaves the tile empty.
+__device__ __forceinline__ TileInfo resolve_tile(const GroupedArgs& a, int64_t row0) {
   const uint32_t* so = a.scales_offsets;
   const int lane = threadIdx.x & 31;
   int lo = 0, hi = a.G;
   while (hi - lo > 256) {
     const int step = (hi - lo + 255) >> 8;
-    bool le[8];
+    int cnt = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t pos = lo + static_cast<int64_t>(step) * (1 + lane + 32 * i);
-      le[i] = pos < hi && static_cast<int64_t>(__ldg(so + pos)) <= row0;
+      cnt += __popc(__ballot_sync(0xFFFFFFFFu, pos < hi && static_cast<int64_t>(__ldg(so + pos)) <= row0));
     }
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cnt += __popc(__ballot_sync(0xFFFFFFFFu, le[i]));
     const int nlo = lo + cnt * step;
     hi = min(hi, nlo + step);
     lo = nlo;
@@ -94,131 +109,265 @@ __device__ __forceinline__ GroupHit warp_group_search(const GroupedArgs& a, int6
   // final round: positions lo+1 .. lo+256 (so / ro up to G, expert ids below G)
   uint32_t so_p[8], ro_p[8];
   int32_t e_p[8];
-  bool le[8];
+  int cnt = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int pos = lo + 1 + lane + 32 * i;
     so_p[i] = pos <= a.G ? __ldg(so + pos) : 0xFFFFFFFFu;
     ro_p[i] = pos <= a.G ? __ldg(a.row_offsets + pos) : 0u;
     e_p[i] = pos < a.G ? __ldg(a.expert_ids + pos) : -1;
-    le[i] = pos < hi && static_cast<int64_t>(so_p[i]) <= row0;
   }
+  const int64_t so0 = __ldg(so), so_end = __ldg(so + a.G);
   const uint32_t so_lo = __ldg(so + lo), ro_lo = __ldg(a.row_offsets + lo);
   const int32_t e_lo = __ldg(a.expert_ids + lo);
-  int cnt = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) cnt += __popc(__ballot_sync(0xFFFFFFFFu, le[i]));
-  // g = lo + cnt; entry g sits at probe index cnt-1, entry g+1 at index cnt
-  GroupHit h;
-  h.so_g = cnt == 0 ? so_lo : warp_pick(so_p, cnt - 1);
-  h.r_beg = cnt == 0 ? ro_lo : warp_pick(ro_p, cnt - 1);
-  h.e = cnt == 0 ? e_lo : warp_pick(e_p, cnt - 1);
-  h.so_n = warp_pick(so_p, cnt);
-  h.r_end = warp_pick(ro_p, cnt);
-  return h;
+  for (int i = 0; i < 8; ++i)
+    cnt += __popc(__ballot_sync(0xFFFFFFFFu, lo + 1 + lane + 32 * i < hi &&
+                                                 static_cast<int64_t>(so_p[i]) <= row0));
+  // g = lo + cnt: entry g sits at probe index cnt-1, entry g+1 at index cnt
+  const int64_t so_g = cnt == 0 ? so_lo : warp_pick(so_p, cnt - 1);
+  const int64_t r_beg = cnt == 0 ? ro_lo : warp_pick(ro_p, cnt - 1);
+  const int e = cnt == 0 ? e_lo : warp_pick(e_p, cnt - 1);
+  const int64_t so_n = warp_pick(so_p, cnt);
+  const int64_t r_end = warp_pick(ro_p, cnt);
+
+  TileInfo t{0, 0, -1};
+  if (so0 != 0 || row0 >= so_end) return t;
+  const int64_t m_g = r_end - r_beg;
+  const int64_t i0 = row0 - so_g;
+  if (m_g < 0 || m_g > so_n - so_g || r_end > a.total_rows) {
+    if (lane == 0) record_error(kErrValue);
+    return t;
+  }
+  if (i0 >= m_g || e < 0) return t;  // padding tile, or a skipped group
+  if (a.sf != nullptr && e >= a.num_experts) {
+    if (lane == 0) record_error(kErrValue);
+    return t;
+  }
+  t.dst0 = r_beg + i0;
+  t.n = static_cast<int>(m_g - i0 < 128 ? m_g - i0 : 128);
+  t.e = e;
+  return t;
 }
 
-struct GroupMeta {
-  int64_t dst0;   // first destination row of this tile
-  int n;          // valid rows in the tile (0: nothing to do)
-  int e;          // expert id
+constexpr int kGtWarps = 8;
+constexpr int kGtThreads = 32 * kGtWarps;
+
+struct GtShared {
+  TileInfo tile;
+  float factor_tab[256];
+  float div6_tab[128];
+  int64_t src[128];  // source row of each tile row, -1 when invalid
 };
 
-template <int FMT, int KT>
-__global__ void __launch_bounds__(kGroupedThreads) grouped_quant_kernel(const GroupedArgs a) {
+// Load one lane's 64-column half-tile segment (valid_cols 64 or 32).
+__device__ __forceinline__ void load_row_segment(const uint16_t* p, int valid_cols, bool vec32,
+                                                 uint4 (&v)[8]) {
+  if (vec32) {
+    ld_global_nc_v8(p, v[0], v[1]);
+    ld_global_nc_v8(p + 16, v[2], v[3]);
+    if (valid_cols == 64) {
+      ld_global_nc_v8(p + 32, v[4], v[5]);
+      ld_global_nc_v8(p + 48, v[6], v[7]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
+    if (valid_cols == 64) {
+#pragma unroll
+      for (int c = 4; c < 8; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
+    }
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kGtThreads) grouped_tile_kernel(const GroupedArgs a) {
+  __shared__ GtShared sh;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+
+  if (warp == 0) {
+    const TileInfo t = resolve_tile(a, static_cast<int64_t>(tile) * 128);
+    if (lane == 0) {
+      sh.tile = t;
+      if (tile == 0 && blockIdx.y == 0) check_offsets(a);
+    }
+  } else if (FMT == kNVFP4) {
+    fill_div6_table(sh.div6_tab, threadIdx.x - 32, kGtThreads - 32);
+  }
+  __syncthreads();
+  const TileInfo t = sh.tile;
+  if (t.n == 0) return;
+
+  // tile rows' sources (and the NVFP4 element-scale table of the expert)
+  if (threadIdx.x < 128) {
+    int64_t src = -1;
+    if (static_cast<int>(threadIdx.x) < t.n) {
+      const int64_t d = t.dst0 + threadIdx.x;
+      src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
+      if (src < 0 || src >= a.in_rows) {
+        record_error(kErrValue);
+        src = -1;
+      }
+    }
+    sh.src[threadIdx.x] = src;
+  }
+  float tsf = 1.0f;
+  if constexpr (FMT == kNVFP4) {
+    tsf = __ldg(a.sf + t.e);
+    fill_nvfp4_factor_table(sh.factor_tab, tsf, threadIdx.x, kGtThreads);
+  }
+  __syncthreads();
+
+  // lane -> (row, 64-column half) as in the dense kernel
+  const int h = warp >> 2;
+  const int r32 = 8 * (warp & 3) + (lane & 7);
+  const int r4 = lane >> 3;
+  const int row = r32 + 32 * r4;
+  const int64_t src = sh.src[row];
+  if (row >= t.n || src < 0) return;
+  const NvScale ns{tsf, sh.factor_tab, nullptr, sh.div6_tab};
+  const uint16_t* in_row = a.in + src * a.ld_in;
+  uint8_t* out_row = a.out + (t.dst0 + row) * a.out_ld;
+  uint8_t* band = a.scales + static_cast<int64_t>(tile) * a.kt_atoms * 512 + r32 * 16 + r4 * 4;
+
+  const int kt_beg = blockIdx.y * a.ktc;
+  const int kt_end = min(a.tiles_k, kt_beg + a.ktc);
+  uint4 buf[2][8];
+  int col0 = kt_beg * 128 + 64 * h;
+  if (col0 < a.K) load_row_segment(in_row + col0, min(64, a.K - col0), a.in_vec32 != 0, buf[0]);
+#pragma unroll 1
+  for (int kt = kt_beg; kt < kt_end; ++kt) {
+    const int cur = (kt - kt_beg) & 1;
+    col0 = kt * 128 + 64 * h;
+    const int ncol0 = col0 + 128;
+    if (kt + 1 < kt_end && ncol0 < a.K) {
+      if (cur == 0) load_row_segment(in_row + ncol0, min(64, a.K - ncol0), a.in_vec32 != 0, buf[1]);
+      else load_row_segment(in_row + ncol0, min(64, a.K - ncol0), a.in_vec32 != 0, buf[0]);
+    }
+    if (col0 < a.K) {
+      uint8_t* dst = out_row + (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0);
+      const uint32_t sbytes = cur == 0
+          ? quant_box_regs<FMT>(buf[0], min(64, a.K - col0), dst, a.out_vec32 != 0, ns)
+          : quant_box_regs<FMT>(buf[1], min(64, a.K - col0), dst, a.out_vec32 != 0, ns);
+      if constexpr (FMT == kNVFP4) {
+        *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
+      } else {
+        *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = static_cast<uint16_t>(sbytes);
+      }
+    } else if constexpr (FMT != kNVFP4) {
+      *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = 0;  // atom's blocks beyond K
+    }
+  }
+}
+
+// ------------------------------------------------------ grouped_rows_kernel --
+
+constexpr int kGrWarps = 4;
+constexpr int kGrThreads = 32 * kGrWarps;
+
+// Per-row state of a warp's rows, in shared memory so that any lane can read
+// the row of the block it holds.
+struct alignas(16) RowState {
+  int64_t src;     // source row (input)
+  int64_t dst;     // destination row (packed output)
+  int64_t band;    // byte offset of the 5D row band of the scale row
+  int atom_off;    // (srow % 32) * 16 + ((srow % 128) / 32) * 4
+  int ok;          // quantize this row
+  float tsf;
+};
+
+template <int FMT, int KT, int R>
+__global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedArgs a) {
+  static_assert(R <= 32, "one lane per row");
   constexpr int SF = Fmt<FMT>::SF;
-  constexpr int BPR = 4 * KT;                      // scale blocks per row in a chunk
+  constexpr int BPR = 4 * KT;                       // scale blocks per row in a run
   constexpr int LOG_BPR = KT == 1 ? 2 : KT == 2 ? 3 : KT == 4 ? 4 : 5;
-  constexpr int U = FMT == kMXFP8 ? 2 : 4;         // blocks in flight per thread
+  constexpr int SLOTS = (R * BPR + 31) / 32;        // blocks per lane
+  constexpr int U = FMT != kNVFP4 ? (SLOTS < 4 ? SLOTS : 4) : (SLOTS < 8 ? SLOTS : 8);
 
-  __shared__ GroupMeta meta;
-  __shared__ float factor_tab[FMT == kNVFP4 ? 256 : 1];
-  __shared__ float div6_tab[FMT == kNVFP4 ? 128 : 1];
+  __shared__ RowState rs_all[kGrWarps][R];
+  __shared__ float div6_tab[128];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if constexpr (FMT == kNVFP4) fill_div6_table(div6_tab, threadIdx.x, kGrThreads);
+  __syncthreads();
 
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 128;
-  if (threadIdx.x < 32) {
-    // ---- warp 0: locate the group
-    GroupMeta m{0, 0, -1};
-    const GroupHit h = warp_group_search(a, row0);
-    const int64_t so0 = __ldg(a.scales_offsets), so_end = __ldg(a.scales_offsets + a.G);
-    const int64_t ro_end = __ldg(a.row_offsets + a.G);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
-        (so0 != 0 || so_end > a.total_scale_rows || ro_end > a.total_rows))
-      record_error(kErrValue);
-    if (so0 == 0 && row0 < so_end) {
-      const int64_t m_g = h.r_end - h.r_beg;
-      const int64_t i0 = row0 - h.so_g;
-      if (m_g < 0 || m_g > h.so_n - h.so_g || h.r_end > a.total_rows) {
-        if (threadIdx.x == 0) record_error(kErrValue);
-      } else if (i0 < m_g && h.e >= 0) {
-        if (FMT == kNVFP4 && h.e >= a.num_experts) {
-          if (threadIdx.x == 0) record_error(kErrValue);
+  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kGrWarps + warp) * R;
+  if (d0 >= a.total_rows) return;
+  RowState* rs = rs_all[warp];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_offsets(a);
+
+  // ---- lane r resolves row d0 + r
+  if (lane < R) {
+    const int64_t d = d0 + lane;
+    RowState st{d, d, 0, 0, 0, 1.0f};
+    const int64_t ro_end = d < a.total_rows ? static_cast<int64_t>(__ldg(a.row_offsets + a.G)) : 0;
+    if (d < ro_end) {
+      // g = max{g : ro[g] <= d}: binary search for the first ro[g+1] > d
+      int lo = 0, hi = a.G - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(a.row_offsets + mid + 1)) <= d) lo = mid + 1;
+        else hi = mid;
+      }
+      const int64_t r_beg = __ldg(a.row_offsets + lo), r_end = __ldg(a.row_offsets + lo + 1);
+      const int64_t so_g = __ldg(a.scales_offsets + lo), so_n = __ldg(a.scales_offsets + lo + 1);
+      const int e = __ldg(a.expert_ids + lo);
+      const int64_t srow = so_g + (d - r_beg);
+      if (r_end - r_beg < 0 || r_end - r_beg > so_n - so_g || r_end > a.total_rows ||
+          srow >= a.total_scale_rows || d < r_beg || (a.sf != nullptr && e >= a.num_experts)) {
+        record_error(kErrValue);
+      } else if (e >= 0) {
+        const int64_t src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
+        if (src < 0 || src >= a.in_rows) {
+          record_error(kErrValue);
         } else {
-          m.dst0 = h.r_beg + i0;
-          m.n = static_cast<int>(m_g - i0 < 128 ? m_g - i0 : 128);
-          m.e = h.e;
+          st.src = src;
+          st.band = (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512;
+          st.atom_off = static_cast<int>((srow & 31) * 16 + ((srow & 127) >> 5) * 4);
+          st.ok = 1;
+          if (a.sf != nullptr) st.tsf = __ldg(a.sf + e);
         }
       }
     }
-    if (threadIdx.x == 0) meta = m;
-  } else if (FMT == kNVFP4) {
-    fill_div6_table(div6_tab, threadIdx.x - 32, kGroupedThreads - 32);
+    rs[lane] = st;
   }
-  __syncthreads();
-  const GroupMeta m = meta;
-  if (m.n == 0) return;
+  __syncwarp();
 
+  // ---- quantize the warp's (row, block) slots
   const int atom0 = blockIdx.y * KT;
   const int col_base = atom0 * 4 * SF;
-  const int total = m.n << LOG_BPR;
-  uint8_t* band = a.scales + static_cast<int64_t>(blockIdx.x) * a.kt_atoms * 512;
-  float tsf = 1.0f;
-
-  for (int base = 0; base < total; base += kGroupedThreads * U) {
+#pragma unroll
+  for (int j0 = 0; j0 < SLOTS; j0 += U) {
     uint4 v[U][SF / 8];
     bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int q = base + u * kGroupedThreads + threadIdx.x;
+      const int q = (j0 + u) * 32 + lane;
       const int r = q >> LOG_BPR;
       const int col = col_base + (q & (BPR - 1)) * SF;
 #pragma unroll
       for (int c = 0; c < SF / 8; ++c) v[u][c] = make_uint4(0u, 0u, 0u, 0u);
-      ok[u] = false;
-      if (q < total && col < a.K) {
-        const int64_t d = m.dst0 + r;
-        const int64_t src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
-        if (src >= 0 && src < a.in_rows) {
-          const uint16_t* p = a.in + src * a.ld_in + col;
-          if (a.in_vec32) {
+      ok[u] = r < R && col < a.K && rs[r < R ? r : 0].ok;
+      if (ok[u]) {
+        const uint16_t* p = a.in + rs[r].src * a.ld_in + col;
+        if (a.in_vec32) {
 #pragma unroll
-            for (int c = 0; c < SF / 8; c += 2) ld_global_nc_v8(p + 8 * c, v[u][c], v[u][c + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < SF / 8; ++c) v[u][c] = ld_global_nc_v4(p + 8 * c);
-          }
-          ok[u] = true;
+          for (int c = 0; c < SF / 8; c += 2) ld_global_nc_v8(p + 8 * c, v[u][c], v[u][c + 1]);
         } else {
-          record_error(kErrValue);
+#pragma unroll
+          for (int c = 0; c < SF / 8; ++c) v[u][c] = ld_global_nc_v4(p + 8 * c);
         }
-      }
-    }
-    if constexpr (FMT == kNVFP4) {
-      if (base == 0) {
-        // the expert's tensor_sf and element-scale table, while the first
-        // round of gathered loads is in flight
-        tsf = __ldg(a.sf + m.e);
-        fill_nvfp4_factor_table(factor_tab, tsf, threadIdx.x, kGroupedThreads);
-        __syncthreads();
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int q = base + u * kGroupedThreads + threadIdx.x;
-      const int r = q >> LOG_BPR;
+      const int q = (j0 + u) * 32 + lane;
+      const int r = (q >> LOG_BPR) < R ? (q >> LOG_BPR) : 0;
       const int b = q & (BPR - 1);
       const int col = col_base + b * SF;
-
       uint32_t acc = 0;
 #pragma unroll
       for (int c = 0; c < SF / 8; ++c) {
@@ -226,11 +375,11 @@ __global__ void __launch_bounds__(kGroupedThreads) grouped_quant_kernel(const Gr
         acc = absmax2(acc, v[u][c].z); acc = absmax2(acc, v[u][c].w);
       }
       const float amax = absmax_final(acc);
+      uint8_t* dst = a.out + rs[r].dst * a.out_ld + (Fmt<FMT>::OUT_BITS == 4 ? col >> 1 : col);
       uint32_t sbyte;
-      const int64_t d = m.dst0 + r;
-      uint8_t* dst = a.out + d * a.out_ld + (Fmt<FMT>::OUT_BITS == 4 ? col >> 1 : col);
       if constexpr (FMT == kNVFP4) {
-        const BlockScale sc = nvfp4_scale_tab(amax, tsf, factor_tab, div6_tab);
+        const NvScale ns{rs[r].tsf, nullptr, nullptr, div6_tab};
+        const BlockScale sc = nvfp4_block_scale(amax, ns);
         sbyte = sc.byte;
         const uint32_t o0 = quant8_e2m1(v[u][0], sc.factor), o1 = quant8_e2m1(v[u][1], sc.factor);
         if (ok[u]) *reinterpret_cast<uint2*>(dst) = make_uint2(o0, o1);
@@ -259,14 +408,13 @@ __global__ void __launch_bounds__(kGroupedThreads) grouped_quant_kernel(const Gr
           }
         }
       }
-
       // scale word of (row r, atom b/4): byte of block b%4 at bits 8*(b%4)
       uint32_t word = sbyte << (8 * (b & 3));
       word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
       word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
       if (ok[u] && (b & 3) == 0) {
         const int atom = atom0 + (b >> 2);
-        *reinterpret_cast<uint32_t*>(band + atom * 512 + (r & 31) * 16 + (r >> 5) * 4) = word;
+        *reinterpret_cast<uint32_t*>(a.scales + rs[r].band + atom * 512 + rs[r].atom_off) = word;
       }
     }
   }

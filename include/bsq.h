@@ -160,6 +160,29 @@ BSQ_API int32_t bsq_grouped_quantize(int32_t fmt, const void* in_dev, int64_t in
                              int64_t total_rows, int64_t total_scale_rows, void* out_dev,
                              void* scales5d_dev, int32_t k_tiles_per_block, void* stream);
 
+/* Kernel of the grouped quantize. */
+typedef enum {
+  BSQ_GROUPED_AUTO = 0,    /* LATENCY when total_rows <= 16 * G, else STREAM */
+  BSQ_GROUPED_STREAM = 1,  /* one thread block per 128-row scale tile (groups of many rows) */
+  BSQ_GROUPED_LATENCY = 2  /* one warp per 2 destination rows (groups of a few rows) */
+} bsq_grouped_kernel;
+
+/*
+ * bsq_grouped_quantize with an explicit kernel choice (bsq_grouped_kernel);
+ * the results are identical whichever kernel runs.  An unknown `kernel`
+ * returns BSQ_ERR_VALUE.
+ */
+BSQ_API int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in_dev, int64_t in_rows,
+                                            int64_t K, int64_t ld_in,
+                                            const uint32_t* row_offsets_dev,
+                                            const uint32_t* scales_offsets_dev,
+                                            const int32_t* expert_ids_dev, const float* sf_dev,
+                                            int32_t num_experts, const int32_t* row_indices_dev,
+                                            int32_t G, int64_t total_rows,
+                                            int64_t total_scale_rows, void* out_dev,
+                                            void* scales5d_dev, int32_t k_tiles_per_block,
+                                            int32_t kernel, void* stream);
+
 /*
  * Rank-2 -> 5D scale reinterleave (block_scales_interleave / _fp4 / _fp4_kernel).
  *

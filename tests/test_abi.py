@@ -145,3 +145,19 @@ def test_binding_raises_readable_errors(lib):
     import fp8_activation_quantization_bsq_gb300 as bsq
     err = bsq.BsqError(SHAPE, "bsq_quantize")
     assert "BSQ_ERR_SHAPE" in str(err) and err.code == SHAPE
+
+
+def test_grouped_kernel_choice_validation(lib):
+    lib.bsq_grouped_quantize_kernel.restype = ctypes.c_int32
+    lib.bsq_grouped_quantize_kernel.argtypes = [
+        ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+
+    def call(kernel, out=P):
+        return lib.bsq_grouped_quantize_kernel(0, P, 64, 256, 256, P, P, P, P, 8, None, 4, 64, 512,
+                                               out, P, 1, kernel, None)
+    assert call(3) == VALUE and call(-1) == VALUE
+    for k in (0, 1, 2):
+        assert call(k, out=None) == NULL      # valid choice: stops at the next check

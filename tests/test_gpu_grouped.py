@@ -30,7 +30,7 @@ def bsq():
 
 
 def _run_grouped(bsq, fmt, d, kt, use_ridx=True, expert_ids=None, x_bits=None, ridx=None,
-                 expect_error=0):
+                 expect_error=0, kernel="auto"):
     x_bits = d["x_bits"] if x_bits is None else x_bits
     K = x_bits.shape[1]
     eid = d["expert_ids"] if expert_ids is None else expert_ids
@@ -45,7 +45,7 @@ def _run_grouped(bsq, fmt, d, kt, use_ridx=True, expert_ids=None, x_bits=None, r
                          torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
                          i32_device(ridx) if ridx is not None else None,
                          total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=kt,
-                         out=out, scales=sc)
+                         out=out, scales=sc, kernel=kernel)
     assert bsq.device_error() == expect_error
     assert margin_intact(ofull) and margin_intact(sfull)
     return out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy()
@@ -63,38 +63,69 @@ def _compare(fmt, d, p, s, use_ridx=True, expert_ids=None, x_bits=None, ridx=Non
     assert np.all(s[~sw] == SENTINEL), "padding scale rows were written"
 
 
+KERNELS = ["stream", "latency"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
 @pytest.mark.parametrize("kt", [1, 2, 4, 8])
 @pytest.mark.parametrize("K", [256, 96, 1120])
-def test_grouped_small(bsq, fmt, kt, K):
+def test_grouped_small(bsq, fmt, kt, K, kernel):
     d = wl.config_grouped_prefill(seed=K + kt, tokens=96, K=K, num_experts=16, top_k=4, fmt=fmt)
-    p, s = _run_grouped(bsq, fmt, d, kt)
+    p, s = _run_grouped(bsq, fmt, d, kt, kernel=kernel)
     _compare(fmt, d, p, s)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+def test_grouped_exhaustive_amax_per_expert(bsq, fmt, kernel):
+    """Every BF16 block amax through the grouped kernels, with a different
+    tensor_sf per expert (NVFP4): scale bytes and codes bit-exact."""
+    from test_gpu_dense import _amax_sweep_matrix
+    SF = oracle.block_size(fmt)
+    mat = _amax_sweep_matrix(SF, per_row_blocks=16)             # 2040 rows x 16 blocks
+    rows = mat.shape[0]
+    G = 24
+    rng = np.random.Generator(np.random.PCG64(77))
+    cuts = np.sort(rng.choice(np.arange(1, rows), G - 1, replace=False))
+    m = np.diff(np.concatenate([[0], cuts, [rows]]))
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = np.concatenate([[0], np.cumsum((m + 127) // 128 * 128)]).astype(np.uint32)
+    sf = np.array([1.0, 0.6640316, 1e-20, 1e20, 2688.0, 3.0e-3] * 8, np.float32)[:G]
+    d = dict(x_bits=mat, row_offsets=ro, scales_offsets=so, expert_ids=np.arange(G, dtype=np.int32),
+             sf_tensor=sf, row_indices=rng.permutation(rows).astype(np.int32),
+             total_rows=rows, total_scale_rows=int(so[-1]), G=G)
+    for kt in (1, 4):
+        p, s = _run_grouped(bsq, fmt, d, kt, kernel=kernel)
+        _compare(fmt, d, p, s)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
-def test_grouped_identity_rows(bsq, fmt):
+def test_grouped_identity_rows(bsq, fmt, kernel):
     d = wl.config_grouped_prefill(seed=1, tokens=64, K=512, num_experts=8, top_k=2, fmt=fmt)
     # without row_indices the destination row d reads source row d
     x = wl.dense_activations(np.random.Generator(np.random.PCG64(2)), d["total_rows"], 512, "blocklognormal")
-    p, s = _run_grouped(bsq, fmt, d, 2, use_ridx=False, x_bits=x)
+    p, s = _run_grouped(bsq, fmt, d, 2, use_ridx=False, x_bits=x, kernel=kernel)
     _compare(fmt, d, p, s, use_ridx=False, x_bits=x)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
-def test_grouped_large_groups_span_tiles(bsq, fmt):
+def test_grouped_large_groups_span_tiles(bsq, fmt, kernel):
     # few experts, many rows each: groups span several 128-row tiles
     d = wl.config_grouped_prefill(seed=9, tokens=600, K=320, num_experts=4, top_k=2, fmt=fmt)
     assert max(np.diff(d["row_offsets"])) > 256
-    p, s = _run_grouped(bsq, fmt, d, 4)
+    p, s = _run_grouped(bsq, fmt, d, 4, kernel=kernel)
     _compare(fmt, d, p, s)
 
 
-def test_grouped_negative_expert_ids_are_skipped(bsq):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_negative_expert_ids_are_skipped(bsq, kernel):
     d = wl.config_grouped_prefill(seed=4, tokens=80, K=256, num_experts=16, top_k=4)
     eid = d["expert_ids"].copy()
     eid[::3] = -1
-    p, s = _run_grouped(bsq, "nvfp4", d, 1, expert_ids=eid)
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, expert_ids=eid, kernel=kernel)
     _compare("nvfp4", d, p, s, expert_ids=eid)
 
 
@@ -111,29 +142,32 @@ def test_grouped_many_groups_search(bsq):
              sf_tensor=np.ones(G, np.float32), row_indices=rng.permutation(int(ro[-1])).astype(np.int32),
              total_rows=int(ro[-1]), total_scale_rows=int(so[-1]), G=G)
     for fmt in ("mxfp8", "nvfp4"):
-        p, s = _run_grouped(bsq, fmt, d, 1)
-        _compare(fmt, d, p, s)
+        for kernel in KERNELS:
+            p, s = _run_grouped(bsq, fmt, d, 1, kernel=kernel)
+            _compare(fmt, d, p, s)
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
 @pytest.mark.parametrize("K", [7168, 2048])
 @pytest.mark.parametrize("kt", [1, 2, 4, 8])
-def test_grouped_decode_full_config(bsq, fmt, K, kt):
+@pytest.mark.parametrize("kernel", ["auto", "stream"])
+def test_grouped_decode_full_config(bsq, fmt, K, kt, kernel):
     """Decode: 64 tokens, top-8 over 256 experts (512 rows, many 1-row
     experts), row_indices gather -- fully compared."""
     d = wl.config_grouped_decode(K=K, fmt=fmt)
     assert d["total_rows"] / d["G"] <= 8
-    p, s = _run_grouped(bsq, fmt, d, kt)
+    p, s = _run_grouped(bsq, fmt, d, kt, kernel=kernel)
     _compare(fmt, d, p, s)
 
 
-def test_grouped_prefill_full_config_sampled(bsq):
+@pytest.mark.parametrize("kernel", ["auto", "latency"])
+def test_grouped_prefill_full_config_sampled(bsq, kernel):
     """Prefill: 4096 tokens, top-8 over 256 experts, K=7168 (32768 rows) at
     the benchmark's launch configuration; the oracle checks sampled groups
     (the largest, the smallest and random ones)."""
     d = wl.config_grouped_prefill()
     kt = 8
-    p, s = _run_grouped(bsq, "nvfp4", d, kt)
+    p, s = _run_grouped(bsq, "nvfp4", d, kt, kernel=kernel)
     m = np.diff(d["row_offsets"].astype(np.int64))
     rng = np.random.Generator(np.random.PCG64(3))
     groups = np.unique(np.concatenate([[np.argmax(m), np.argmin(m)], rng.choice(d["G"], 10, replace=False)]))
@@ -150,13 +184,14 @@ def test_grouped_prefill_full_config_sampled(bsq):
         np.testing.assert_array_equal(s[oracle.offset_5d(mm, ss, Kt)], sd)
 
 
-def test_grouped_bad_row_index_is_reported_not_faulted(bsq):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_bad_row_index_is_reported_not_faulted(bsq, kernel):
     d = wl.config_grouped_prefill(seed=8, tokens=40, K=128, num_experts=8, top_k=2)
     ridx = d["row_indices"].copy()
     bad = [3, len(ridx) - 1]
     ridx[bad[0]] = 10_000_000
     ridx[bad[1]] = -5
-    p, s = _run_grouped(bsq, "nvfp4", d, 1, ridx=ridx, expect_error=4)
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, ridx=ridx, expect_error=4, kernel=kernel)
     p_ref, pw, _, _ = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"],
                                               d["scales_offsets"], d["expert_ids"],
                                               d["sf_tensor"], np.where(ridx < 0, 0, np.minimum(ridx, 39)))
@@ -168,13 +203,14 @@ def test_grouped_bad_row_index_is_reported_not_faulted(bsq):
     assert bsq.device_error() == 0
 
 
-def test_grouped_offsets_beyond_buffers_are_reported(bsq):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_offsets_beyond_buffers_are_reported(bsq, kernel):
     """row_offsets[G] beyond total_rows: the overflowing group is skipped,
     the error word says BSQ_ERR_VALUE and nothing lands past the buffers."""
     d = wl.config_grouped_prefill(seed=8, tokens=40, K=128, num_experts=8, top_k=2)
     d2 = dict(d)
     d2["total_rows"] = d["total_rows"] - 1
-    p, s = _run_grouped(bsq, "nvfp4", d2, 1, expect_error=4)
+    p, s = _run_grouped(bsq, "nvfp4", d2, 1, expect_error=4, kernel=kernel)
     last = d["G"] - 1
     r0 = int(d["row_offsets"][last])
     p_ref, _, _, _ = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"],
