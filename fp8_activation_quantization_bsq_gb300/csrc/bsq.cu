@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "dense_quant.cuh"
 #include "device_common.cuh"
@@ -44,6 +45,25 @@ inline int atom_cols_of(int32_t f) { return 4 * sf_of(f); }
 inline int64_t row_bytes_of(int32_t f, int64_t K) { return f == BSQ_MXFP8 ? K : K / 2; }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Launch with programmatic stream serialization (programmatic dependent
+// launch): the kernel may start while the previous kernel in the stream
+// finishes; each kernel waits (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 template <int FMT>
 void dense_kernel_setup(int fidx, DeviceInfo& d) {
@@ -122,9 +142,10 @@ bsq_status launch_dense(const void* in, int64_t M, int64_t K, int64_t ld_in, voi
   const int fidx = FMT;
   const int64_t resident = static_cast<int64_t>(d->sm_count) * d->dense_ctas_per_sm[fidx];
   const int grid = static_cast<int>(a.num_tiles < resident ? a.num_tiles : resident);
-  dense_quant_tma_kernel<FMT, kDenseStages>
-      <<<grid, kDenseThreads, dense_smem_bytes<kDenseStages>(), stream>>>(map, a);
-  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+  const cudaError_t e = launch_pdl(dense_quant_tma_kernel<FMT, kDenseStages>, dim3(grid),
+                                   dim3(kDenseThreads), dense_smem_bytes<kDenseStages>(), stream,
+                                   map, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 template <int FMT, int KT>
@@ -134,8 +155,9 @@ bsq_status launch_grouped_rows(const GroupedArgs& a, cudaStream_t stream) {
   if (chunks > 65535 || blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   if (blocks == 0) return BSQ_OK;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(chunks));
-  grouped_rows_kernel<FMT, KT, kRowsPerWarp><<<grid, kGrThreads, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl(grouped_rows_kernel<FMT, KT, kRowsPerWarp>, grid, dim3(kGrThreads), 0, stream, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 template <int FMT>
@@ -147,8 +169,8 @@ bsq_status launch_grouped_tiles(GroupedArgs a, int kt, cudaStream_t stream) {
   const int64_t tiles = a.total_scale_rows / 128;
   if (chunks > 65535 || tiles >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
-  grouped_tile_kernel<FMT><<<grid, kGtThreads, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+  const cudaError_t e = launch_pdl(grouped_tile_kernel<FMT>, grid, dim3(kGtThreads), 0, stream, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 template <int FMT>
@@ -299,13 +321,14 @@ int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   dim3 grid(static_cast<unsigned>(bands), static_cast<unsigned>(chunks));
   const int ikt = static_cast<int>(kt_atoms);
+  cudaError_t e;
   if (aligned(in, 16) && ld % 16 == 0 && S % 16 == 0)
-    interleave_kernel<16><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
+    e = launch_pdl(interleave_kernel<16>, grid, dim3(kIlvThreads), 0, st, in, M, S, ld, out, ikt);
   else if (aligned(in, 4) && ld % 4 == 0 && S % 4 == 0)
-    interleave_kernel<4><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
+    e = launch_pdl(interleave_kernel<4>, grid, dim3(kIlvThreads), 0, st, in, M, S, ld, out, ikt);
   else
-    interleave_kernel<1><<<grid, kIlvThreads, 0, st>>>(in, M, S, ld, out, ikt);
-  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+    e = launch_pdl(interleave_kernel<1>, grid, dim3(kIlvThreads), 0, st, in, M, S, ld, out, ikt);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 int32_t bsq_device_error(void* stream, int32_t* code_out) {

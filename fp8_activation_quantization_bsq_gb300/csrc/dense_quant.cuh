@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kDenseThreads)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap);
+      pdl_wait();
+      pdl_trigger();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_parity = 0;  // per-stage bit masks
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(kDenseThreads)
     fill_div6_table(div6_tab, threadIdx.x, 32 * kDenseConsumerWarps);
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kDenseConsumerWarps) : "memory");
   }
+  pdl_wait();
 
   // warp -> box h; lane -> row: r32 = 8*(warp%4) + lane%8, r4 = lane/8,
   // row = r32 + 32*r4, so a warp's 32 scale words fill 128 contiguous bytes.

@@ -238,6 +238,18 @@ __device__ __forceinline__ BlockScale nvfp4_scale_tab(float amax, float tsf, con
 }
 
 // ------------------------------------------------------------------- PTX --
+
+// Programmatic dependent launch.  pdl_wait(): block until the grids this one
+// depends on (the previous kernels in the stream) have completed and their
+// memory is visible; every kernel calls it before its first global memory
+// access, so that only its prologue overlaps the previous kernel's tail (a
+// no-op when the launch was not programmatic).  pdl_trigger(): allow the next
+// kernel in the stream to launch now (it still waits for this grid's
+// completion before touching memory).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

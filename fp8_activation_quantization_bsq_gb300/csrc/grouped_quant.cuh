@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kGtThreads) grouped_tile_kernel(const GroupedA
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
+  pdl_wait();
 
   if (warp == 0) {
     const TileInfo t = resolve_tile(a, static_cast<int64_t>(tile) * 128);
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
   const int lane = threadIdx.x & 31;
   if constexpr (FMT == kNVFP4) fill_div6_table(div6_tab, threadIdx.x, kGrThreads);
   __syncthreads();
+  pdl_wait();
 
   const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kGrWarps + warp) * R;
   if (d0 >= a.total_rows) return;

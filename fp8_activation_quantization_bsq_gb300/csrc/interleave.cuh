@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kIlvThreads)
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int a0 = blockIdx.y * kIlvAtoms;
   const int64_t s0 = static_cast<int64_t>(a0) * 4;
+  pdl_wait();
+  pdl_trigger();
 
   if constexpr (VEC > 1) {
     // every load of the thread is issued before the first shared-memory store
