@@ -27,6 +27,7 @@ constexpr int kMaxDevices = 64;
 // larger groups (prefill) the 128-row tile kernel.
 constexpr int64_t kGroupedLatencyMaxAvgRows = 16;
 constexpr int kRowsPerWarp = 2;
+constexpr int kMinTileCols = 8;  // tile kernel: at least 8 x 128 columns per block
 
 struct DeviceInfo {
   bool ready = false;
@@ -66,6 +67,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 template <int FMT>
+void grouped_tile_setup() {
+  cudaFuncSetAttribute(grouped_tile_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kGtSmemBytes);
+}
+
+template <int FMT>
 void dense_kernel_setup(int fidx, DeviceInfo& d) {
   auto k = dense_quant_tma_kernel<FMT, kDenseStages>;
   const int smem = dense_smem_bytes<kDenseStages>();
@@ -87,6 +94,9 @@ bsq_status device_info(DeviceInfo** out) {
     dense_kernel_setup<kNVFP4>(0, d);
     dense_kernel_setup<kMXFP4>(1, d);
     dense_kernel_setup<kMXFP8>(2, d);
+    grouped_tile_setup<kNVFP4>();
+    grouped_tile_setup<kMXFP4>();
+    grouped_tile_setup<kMXFP8>();
     if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
     d.ready = true;
   }
@@ -162,14 +172,19 @@ bsq_status launch_grouped_rows(const GroupedArgs& a, cudaStream_t stream) {
 
 template <int FMT>
 bsq_status launch_grouped_tiles(GroupedArgs a, int kt, cudaStream_t stream) {
+  DeviceInfo* d = nullptr;
+  if (bsq_status st = device_info(&d); st != BSQ_OK) return st;
   a.tiles_k = static_cast<int>(ceil_div(a.K, 128));
-  const int per = kt * atom_cols_of(FMT) / 128;   // 128-column tiles per block
-  a.ktc = per > 0 ? per : 1;
+  // 128-column tiles per block: k_tiles_per_block atom columns, but at least
+  // kMinTileCols so that the block's group lookup and tables are amortized
+  const int per = kt * atom_cols_of(FMT) / 128;
+  a.ktc = per > kMinTileCols ? per : kMinTileCols;
   const int64_t chunks = ceil_div(a.tiles_k, a.ktc);
   const int64_t tiles = a.total_scale_rows / 128;
   if (chunks > 65535 || tiles >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
-  const cudaError_t e = launch_pdl(grouped_tile_kernel<FMT>, grid, dim3(kGtThreads), 0, stream, a);
+  const cudaError_t e =
+      launch_pdl(grouped_tile_kernel<FMT>, grid, dim3(kGtThreads), kGtSmemBytes, stream, a);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 

@@ -13,10 +13,14 @@
 //    the last round also reads row_offsets and expert_ids at the probe
 //    positions, so up to 256 groups cost one round of loads).  Then, as in
 //    the dense kernel, each lane owns one row and one 64-column half of a
-//    tile, loads its gathered row segment with 256-bit loads (whole 32-byte
-//    sectors per lane), double-buffered across the column tiles, quantizes it
-//    in registers with the block's element-scale table and stores whole
-//    sectors; a warp's 32 scale words form one coalesced 128-byte store.
+//    tile.  Each warp streams its 32 rows' gathered segments into a 3-deep
+//    shared-memory ring with cp.async (8 lanes per row, so each instruction
+//    moves 4 rows x 128 B in whole sectors; two column tiles in flight while
+//    the third is quantized; the warp waits only for its own copy groups, so
+//    the loop has no block barrier), then each lane quantizes its row from
+//    shared memory with the block's element-scale table and stores whole
+//    sectors.  Warps own 32 consecutive rows, so the unused rows of a
+//    partly filled tile are whole warps that leave at once.
 //
 //  * grouped_rows_kernel (groups of a few rows, decode).  A warp owns R
 //    consecutive destination rows and one run of k_tiles_per_block atom
@@ -152,6 +156,10 @@ __device__ __forceinline__ TileInfo resolve_tile(const GroupedArgs& a, int64_t r
 
 constexpr int kGtWarps = 8;
 constexpr int kGtThreads = 32 * kGtWarps;
+constexpr int kGtPitch = 272;                     // bytes per staged row: 2 x 128 + 16 pad
+constexpr int kGtStageBytes = 128 * kGtPitch;
+constexpr int kGtStages = 3;
+constexpr int kGtSmemBytes = kGtStages * kGtStageBytes;
 
 struct GtShared {
   TileInfo tile;
@@ -160,29 +168,21 @@ struct GtShared {
   int64_t src[128];  // source row of each tile row, -1 when invalid
 };
 
-// Load one lane's 64-column half-tile segment (valid_cols 64 or 32).
-__device__ __forceinline__ void load_row_segment(const uint16_t* p, int valid_cols, bool vec32,
-                                                 uint4 (&v)[8]) {
-  if (vec32) {
-    ld_global_nc_v8(p, v[0], v[1]);
-    ld_global_nc_v8(p + 16, v[2], v[3]);
-    if (valid_cols == 64) {
-      ld_global_nc_v8(p + 32, v[4], v[5]);
-      ld_global_nc_v8(p + 48, v[6], v[7]);
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
-    if (valid_cols == 64) {
-#pragma unroll
-      for (int c = 4; c < 8; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
-    }
-  }
+// 16-byte asynchronous global -> shared copy, cached in L2 only.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kGtThreads) grouped_tile_kernel(const GroupedArgs a) {
+__global__ void __launch_bounds__(kGtThreads, 2) grouped_tile_kernel(const GroupedArgs a) {
   __shared__ GtShared sh;
+  extern __shared__ __align__(128) uint8_t ring[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
@@ -221,45 +221,67 @@ __global__ void __launch_bounds__(kGtThreads) grouped_tile_kernel(const GroupedA
   }
   __syncthreads();
 
-  // lane -> (row, 64-column half) as in the dense kernel
+  // warp -> (64-column half h, rows 32*(warp%4) ...+31); lane -> one row
   const int h = warp >> 2;
-  const int r32 = 8 * (warp & 3) + (lane & 7);
-  const int r4 = lane >> 3;
-  const int row = r32 + 32 * r4;
-  const int64_t src = sh.src[row];
-  if (row >= t.n || src < 0) return;
+  const int wr = 32 * (warp & 3);                  // first tile row of this warp
+  if (wr >= t.n) return;                           // no block barrier follows
+  const int row = wr + lane;
+  const bool row_ok = row < t.n && sh.src[row] >= 0;
   const NvScale ns{tsf, sh.factor_tab, nullptr, sh.div6_tab};
-  const uint16_t* in_row = a.in + src * a.ld_in;
   uint8_t* out_row = a.out + (t.dst0 + row) * a.out_ld;
-  uint8_t* band = a.scales + static_cast<int64_t>(tile) * a.kt_atoms * 512 + r32 * 16 + r4 * 4;
+  uint8_t* band = a.scales + static_cast<int64_t>(tile) * a.kt_atoms * 512 + lane * 16 + (warp & 3) * 4;
+
+  // copy role: in copy k (0..7) lane l moves chunk l%8 of row wr + l/8 + 4k
+  const int cc = lane & 7;
+  int64_t csrc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int crow = wr + (lane >> 3) + 4 * k;
+    csrc[k] = crow < t.n ? sh.src[crow] : -1;
+  }
 
   const int kt_beg = blockIdx.y * a.ktc;
   const int kt_end = min(a.tiles_k, kt_beg + a.ktc);
-  uint4 buf[2][8];
-  int col0 = kt_beg * 128 + 64 * h;
-  if (col0 < a.K) load_row_segment(in_row + col0, min(64, a.K - col0), a.in_vec32 != 0, buf[0]);
+  // one copy group per column tile (empty beyond K) keeps wait_group exact
+  auto issue = [&](int kt) {
+    const int col0 = kt * 128 + 64 * h;
+    if (col0 < a.K && cc < (a.K - col0) / 8) {
+      uint8_t* stage = ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + h * 128 + 16 * cc;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int crow = wr + (lane >> 3) + 4 * k;
+        if (csrc[k] >= 0) cp_async16(stage + crow * kGtPitch, a.in + csrc[k] * a.ld_in + col0 + 8 * cc);
+      }
+    }
+    cp_async_commit();
+  };
+  issue(kt_beg);
+  if (kt_beg + 1 < kt_end) issue(kt_beg + 1);
 #pragma unroll 1
   for (int kt = kt_beg; kt < kt_end; ++kt) {
-    const int cur = (kt - kt_beg) & 1;
-    col0 = kt * 128 + 64 * h;
-    const int ncol0 = col0 + 128;
-    if (kt + 1 < kt_end && ncol0 < a.K) {
-      if (cur == 0) load_row_segment(in_row + ncol0, min(64, a.K - ncol0), a.in_vec32 != 0, buf[1]);
-      else load_row_segment(in_row + ncol0, min(64, a.K - ncol0), a.in_vec32 != 0, buf[0]);
-    }
+    const int ahead = min(2, kt_end - 1 - kt);  // groups committed after tile kt
+    if (kt + 2 < kt_end) issue(kt + 2);         // into the slot freed two tiles ago
+    if (ahead >= 2) cp_async_wait<2>();
+    else if (ahead == 1) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncwarp();                               // the warp's copies are visible to all its lanes
+    const int col0 = kt * 128 + 64 * h;
     if (col0 < a.K) {
-      uint8_t* dst = out_row + (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0);
-      const uint32_t sbytes = cur == 0
-          ? quant_box_regs<FMT>(buf[0], min(64, a.K - col0), dst, a.out_vec32 != 0, ns)
-          : quant_box_regs<FMT>(buf[1], min(64, a.K - col0), dst, a.out_vec32 != 0, ns);
-      if constexpr (FMT == kNVFP4) {
-        *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
-      } else {
-        *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = static_cast<uint16_t>(sbytes);
+      if (row_ok) {
+        uint8_t* dst = out_row + (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0);
+        const uint32_t sbytes = quant_box_row<FMT, false>(
+            ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + row * kGtPitch + h * 128, row,
+            min(64, a.K - col0), dst, a.out_vec32 != 0, ns);
+        if constexpr (FMT == kNVFP4) {
+          *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
+        } else {
+          *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = static_cast<uint16_t>(sbytes);
+        }
       }
     } else if constexpr (FMT != kNVFP4) {
-      *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = 0;  // atom's blocks beyond K
+      if (row_ok) *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = 0;  // blocks beyond K
     }
+    __syncwarp();                               // slot reads done before it is refilled
   }
 }
 

@@ -146,7 +146,9 @@ BSQ_API int32_t bsq_quantize(int32_t fmt, const void* in_dev, int64_t M, int64_t
  *                       written row gets all ceil(S/4)*4 scale bytes (padding
  *                       columns 0x00); padding rows are not written.
  *   k_tiles_per_block   1, 2, 4 or 8 column tiles (64 columns for NVFP4, 128
- *                       for MX) handled by one thread block.
+ *                       for MX) handled by one unit of work (a warp of the
+ *                       latency kernel; the streaming kernel's thread blocks
+ *                       take at least 1024 columns).
  * Device checks (error word BSQ_ERR_VALUE, the affected rows are skipped):
  * a source row index outside [0, in_rows); row_offsets[G] > total_rows;
  * scales_offsets[G] > total_scale_rows; scales_offsets[0] != 0; a group with

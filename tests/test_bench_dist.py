@@ -1,0 +1,60 @@
+"""The multi-rank bench harness on CPU: world_size-2 gloo ranks exercise
+bench.py's rank handling (env parsing, barrier, max over ranks) without a
+GPU.  Each rank quantizes its own batch in the real run (weak scaling, no
+collective on the data path); only the timing aggregation is collective."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    r, w, lr = bench.dist_env()
+    dist.init_process_group("gloo", rank=r, world_size=w)
+    bench.barrier(w)
+    mx = bench.max_over_ranks(1.5 + rank, w)     # rank 1 is the slow one
+    bench.barrier(w)
+    dist.destroy_process_group()
+    q.put((r, w, lr, mx))
+
+
+def test_two_rank_max_over_ranks_and_barrier():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 2, 0, 2.5), (1, 2, 1, 2.5)]
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+    bench.barrier(1)
+
+
+def test_reference_arm_rank_gate(monkeypatch, capsys):
+    """Under torchrun only rank 0 runs the reference arm; other ranks exit
+    quietly without work."""
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
