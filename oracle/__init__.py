@@ -34,6 +34,9 @@ the readings taken are:
 * 5D TCGEN scale layout (Mt, Kt, 32, 4, 4): byte of (row m, scale column s)
   at ((m/128)*Kt + s/4)*512 + (m%32)*16 + ((m%128)/32)*4 + s%4, padding
   entries of the dense output 0x00;
+* tensor scale (computed on the GPU before quantizing): ``tensor_sf =
+  fl32(448*6 / amax)``, amax the exact max |x| (per expert over its gathered
+  rows), 1.0 for an all-zero tensor;
 * grouped: ``row_offsets``/``scales_offsets`` are uint32 prefix sums of
   length G+1 (``scales_offsets`` in rows, multiples of 128), groups with a
   negative expert id are skipped, padding scale rows are not written.
@@ -57,6 +60,7 @@ from .blockquant import (FORMATS, block_size, packed_row_bytes, quantize_rank2,
 from .layout import (scales5d_bytes, offset_5d, scales_to_5d, scales_interleave,
                      scales_from_5d_view)
 from .check import naive_block_scaled_matmul
+from .tensor_scale import tensor_sf, expert_tensor_sf
 
 __all__ = [
     "E2M1_MAGNITUDES", "E4M3_MAGNITUDES", "e2m1_decode", "e4m3_decode", "e8m0_decode",
@@ -64,5 +68,5 @@ __all__ = [
     "packed_row_bytes", "quantize_rank2", "quantize", "grouped_quantize", "dequantize",
     "scales5d_bytes", "offset_5d", "scales_to_5d", "scales_interleave",
     "scales_from_5d_view", "naive_block_scaled_matmul", "nvfp4_block_scale",
-    "nvfp4_element_scale", "mx_block_exponent",
+    "nvfp4_element_scale", "mx_block_exponent", "tensor_sf", "expert_tensor_sf",
 ]
