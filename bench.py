@@ -233,6 +233,28 @@ def extra_workloads(bsq, device, flush, peak):
     res["nvfp4_dense_M128_K256"] = {"us": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
                                     "GB_s": round(dense_bytes("nvfp4", 128, 256) / (mean * 1e6), 1)}
 
+    # tensor-scale reduction and the on-device NVFP4 chain (tensor_sf, then
+    # quantize reading it from device memory) on the 8192 x 7168 activations
+    c = wl.config_dense_nvfp4_large()
+    x = to_dev_bf16(c["x_bits"], device)
+    M, K = c["x_bits"].shape
+    del c
+    ws = torch.empty(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
+    tsf = bsq.tensor_sf(x, workspace=ws)
+    mean, mn = time_events(lambda: bsq.tensor_sf(x, out=tsf, workspace=ws), reps, flush)
+    res[f"tensor_sf_M{M}_K{K}"] = {"us": round(mean * 1e3, 2), "GB_s": round(M * K * 2 / (mean * 1e6), 1),
+                                   "frac_of_hbm": round(M * K * 2 / (mean * 1e6) / peak, 3)}
+    out, sc = bsq.quantize_dynamic(x, "nvfp4", tsf[1:])
+
+    def chain():
+        bsq.tensor_sf(x, out=tsf, workspace=ws)
+        bsq.quantize_dynamic(x, "nvfp4", tsf[1:], out=out, scales=sc)
+    mean, mn = time_events(chain, reps, flush)
+    res[f"nvfp4_dynamic_chain_M{M}_K{K}"] = {
+        "us": round(mean * 1e3, 2), "note": "tensor_sf + quantize_dynamic; the input is read twice",
+        "GB_s_of_quantize_bytes": round(dense_bytes("nvfp4", M, K) / (mean * 1e6), 1)}
+    del x, out, sc
+
     c = wl.config_dense_mx_wide()
     x = to_dev_bf16(c["x_bits"], device)
     del c
@@ -271,6 +293,18 @@ def extra_workloads(bsq, device, flush, peak):
 
     d = wl.config_grouped_prefill()
     uniq = int(np.unique(d["row_indices"]).size)
+    xg = to_dev_bf16(d["x_bits"], device)
+    ro = torch.from_numpy(np.ascontiguousarray(d["row_offsets"], np.uint32).view(np.int32)).to(device)
+    eid = torch.from_numpy(d["expert_ids"]).to(device)
+    ridx = torch.from_numpy(d["row_indices"]).to(device)
+    E = d["num_experts"]
+    gws = torch.empty(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device=device)
+    gsf = bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], workspace=gws)
+    mean, mn = time_events(lambda: bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"],
+                                                         out=gsf, workspace=gws), reps, flush)
+    res["grouped_tensor_sf_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2),
+                                                    "gathered_GB_s": round(d["total_rows"] * d["K"] * 2 / (mean * 1e6), 1)}
+    del xg, gsf, gws
     for kt in (8,):
         mean, mn, b = grouped(d, "nvfp4", kt, "prefill", uniq)
         res[f"nvfp4_grouped_prefill_T4096_K7168_kt{kt}"] = {

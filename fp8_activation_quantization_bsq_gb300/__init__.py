@@ -22,8 +22,9 @@ import torch
 
 from ._build import LIB_PATH
 
-__all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes", "scales5d_bytes",
-           "quantize", "grouped_quantize", "scales_interleave", "device_error", "status_string"]
+__all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes",
+           "scales5d_bytes", "quantize", "quantize_dynamic", "tensor_sf", "grouped_tensor_sf",
+           "grouped_quantize", "scales_interleave", "device_error", "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
 GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2}
@@ -44,6 +45,12 @@ _SIGNATURES = {
                                              _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64,
                                              _c_p, _c_p, _c_i32, _c_i32, _c_p]),
     "bsq_scales_interleave": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
+    "bsq_quantize_dynamic": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p]),
+    "bsq_tensor_sf_workspace_bytes": (_c_i64, []),
+    "bsq_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p]),
+    "bsq_grouped_tensor_sf_workspace_bytes": (_c_i64, [_c_i32]),
+    "bsq_grouped_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i32,
+                                       _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p]),
     "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),
 }
 
@@ -125,6 +132,72 @@ def quantize(x: torch.Tensor, fmt, tensor_sf: float = 1.0, out=None, scales=None
                                 float(tensor_sf), _stream(x.device, stream))
     _check(rc, "bsq_quantize")
     return out, scales
+
+
+def quantize_dynamic(x: torch.Tensor, fmt, tensor_sf_dev=None, out=None, scales=None, stream=None):
+    """Like ``quantize`` with the NVFP4 tensor_sf read from device memory
+    (``tensor_sf_dev``: a float32 CUDA tensor whose first element is used,
+    e.g. ``tensor_sf(x)[1:]``).  When it is None (NVFP4), the scale is computed
+    first on the GPU with ``tensor_sf``; nothing waits for the host."""
+    _check_x(x)
+    f = _fmt(fmt)
+    M, K = x.shape
+    if f == FORMATS["nvfp4"] and tensor_sf_dev is None:
+        tensor_sf_dev = tensor_sf(x, stream=stream)[1:]
+    if out is None:
+        out = torch.empty((M, packed_row_bytes(f, K)), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(scales5d_bytes(f, M, K), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().bsq_quantize_dynamic(f, _ptr(x), M, K, x.stride(0) if M else K, _ptr(out),
+                                        _ptr(scales), _ptr(tensor_sf_dev), _stream(x.device, stream))
+    _check(rc, "bsq_quantize_dynamic")
+    return out, scales
+
+
+def tensor_sf(x: torch.Tensor, out=None, workspace=None, stream=None):
+    """float32 CUDA tensor [amax, tensor_sf] of a 2-D BF16 CUDA tensor,
+    tensor_sf = fl32(448*6/amax) (1.0 for an all-zero tensor)."""
+    _check_x(x)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(2, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().bsq_tensor_sf(_ptr(x), M, K, x.stride(0) if M else K, _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(x.device, stream))
+    _check(rc, "bsq_tensor_sf")
+    return out
+
+
+def grouped_tensor_sf(x: torch.Tensor, row_offsets, expert_ids, num_experts: int,
+                      row_indices=None, total_rows: int | None = None, out=None, workspace=None,
+                      stream=None):
+    """float32 CUDA tensor [num_experts] of per-expert tensor scales over the
+    experts' gathered rows (1.0 for experts without rows)."""
+    _check_x(x)
+    in_rows, K = x.shape
+    G = expert_ids.numel()
+    if total_rows is None:
+        total_rows = row_indices.numel() if row_indices is not None else in_rows
+    if out is None:
+        out = torch.empty(num_experts, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(lib().bsq_grouped_tensor_sf_workspace_bytes(num_experts),
+                                dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().bsq_grouped_tensor_sf(_ptr(x), in_rows, K, x.stride(0) if in_rows else K,
+                                         _ptr(row_offsets), _ptr(expert_ids), _ptr(row_indices), G,
+                                         total_rows, _ptr(out), num_experts, _ptr(workspace),
+                                         workspace.numel(), _stream(x.device, stream))
+    _check(rc, "bsq_grouped_tensor_sf")
+    return out
+
+
+def _check_x(x):
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
 
 
 def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_ids,

@@ -13,7 +13,8 @@ LIB_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libbsq.so")
 
 SOURCES = ["bsq.cu"]
-HEADERS = ["device_common.cuh", "dense_quant.cuh", "grouped_quant.cuh", "interleave.cuh"]
+HEADERS = ["device_common.cuh", "box_quant.cuh", "dense_quant.cuh", "grouped_quant.cuh", "interleave.cuh",
+           "tensor_scale.cuh"]
 
 
 def nvcc_path() -> str:

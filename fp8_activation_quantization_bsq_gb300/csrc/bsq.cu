@@ -9,12 +9,14 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <algorithm>
 #include <utility>
 
 #include "dense_quant.cuh"
 #include "device_common.cuh"
 #include "grouped_quant.cuh"
 #include "interleave.cuh"
+#include "tensor_scale.cuh"
 
 namespace {
 
@@ -120,7 +122,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 
 template <int FMT>
 bsq_status launch_dense(const void* in, int64_t M, int64_t K, int64_t ld_in, void* out,
-                        void* scales, float tsf, cudaStream_t stream) {
+                        void* scales, float tsf, const float* tsf_dev, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
   auto enc = encode_tiled();
@@ -148,6 +150,7 @@ bsq_status launch_dense(const void* in, int64_t M, int64_t K, int64_t ld_in, voi
   a.kt_atoms = static_cast<int>(ceil_div(K, atom_cols_of(FMT)));
   a.vec32 = (a.out_ld % 32 == 0) && aligned(out, 32);
   a.tsf = tsf;
+  a.tsf_dev = tsf_dev;
 
   const int fidx = FMT;
   const int64_t resident = static_cast<int64_t>(d->sm_count) * d->dense_ctas_per_sm[fidx];
@@ -232,24 +235,131 @@ int64_t bsq_scales5d_bytes(int32_t fmt, int64_t rows, int64_t K) {
   return ceil_div(rows, 128) * ceil_div(K / sf_of(fmt), 4) * 512;
 }
 
-int32_t bsq_quantize(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in, void* out,
-                     void* scales, float tensor_sf, void* stream) {
+namespace {
+bsq_status check_dense(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in,
+                       const void* out, const void* scales, bool* noop) {
+  *noop = false;
   if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
   if (M < 0 || K < 0 || K % 32 != 0 || M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
     return BSQ_ERR_SHAPE;
-  if (M == 0 || K == 0) return BSQ_OK;
+  if (M == 0 || K == 0) {
+    *noop = true;
+    return BSQ_OK;
+  }
   if (ld_in < K) return BSQ_ERR_SHAPE;
   if (ceil_div(M, 128) * ceil_div(K, 128) >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   if (!in || !out || !scales) return BSQ_ERR_NULL;
   if (!aligned(in, 16) || !aligned(out, 16) || !aligned(scales, 16) || ld_in % 8 != 0)
     return BSQ_ERR_ALIGN;
-  if (fmt == BSQ_NVFP4 && !(std::isfinite(tensor_sf) && tensor_sf > 0.0f)) return BSQ_ERR_VALUE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return BSQ_OK;
+}
+
+bsq_status dense_dispatch(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in,
+                          void* out, void* scales, float tsf, const float* tsf_dev,
+                          cudaStream_t st) {
   switch (fmt) {
-    case BSQ_NVFP4: return launch_dense<kNVFP4>(in, M, K, ld_in, out, scales, tensor_sf, st);
-    case BSQ_MXFP4: return launch_dense<kMXFP4>(in, M, K, ld_in, out, scales, 1.0f, st);
-    default: return launch_dense<kMXFP8>(in, M, K, ld_in, out, scales, 1.0f, st);
+    case BSQ_NVFP4: return launch_dense<kNVFP4>(in, M, K, ld_in, out, scales, tsf, tsf_dev, st);
+    case BSQ_MXFP4: return launch_dense<kMXFP4>(in, M, K, ld_in, out, scales, 1.0f, nullptr, st);
+    default: return launch_dense<kMXFP8>(in, M, K, ld_in, out, scales, 1.0f, nullptr, st);
   }
+}
+}  // namespace
+
+int32_t bsq_quantize(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in, void* out,
+                     void* scales, float tensor_sf, void* stream) {
+  bool noop = false;
+  if (bsq_status s = check_dense(fmt, in, M, K, ld_in, out, scales, &noop); s != BSQ_OK || noop)
+    return s;
+  if (fmt == BSQ_NVFP4 && !(std::isfinite(tensor_sf) && tensor_sf > 0.0f)) return BSQ_ERR_VALUE;
+  return dense_dispatch(fmt, in, M, K, ld_in, out, scales, tensor_sf, nullptr,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int32_t bsq_quantize_dynamic(int32_t fmt, const void* in, int64_t M, int64_t K, int64_t ld_in,
+                             void* out, void* scales, const float* tensor_sf_dev, void* stream) {
+  bool noop = false;
+  if (bsq_status s = check_dense(fmt, in, M, K, ld_in, out, scales, &noop); s != BSQ_OK || noop)
+    return s;
+  if (fmt == BSQ_NVFP4 && !tensor_sf_dev) return BSQ_ERR_NULL;
+  if (fmt == BSQ_NVFP4 && !aligned(tensor_sf_dev, 4)) return BSQ_ERR_ALIGN;
+  return dense_dispatch(fmt, in, M, K, ld_in, out, scales, 1.0f,
+                        fmt == BSQ_NVFP4 ? tensor_sf_dev : nullptr,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int64_t bsq_tensor_sf_workspace_bytes(void) { return static_cast<int64_t>(sizeof(AmaxWorkspace)); }
+
+int32_t bsq_tensor_sf(const void* in, int64_t M, int64_t K, int64_t ld_in, float* out,
+                      void* workspace, int64_t workspace_bytes, void* stream) {
+  if (M < 0 || K < 0 || K % 8 != 0 || K >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  if (M > 0 && K > 0 && ld_in < K) return BSQ_ERR_SHAPE;
+  if (!out || !workspace || (M > 0 && K > 0 && !in)) return BSQ_ERR_NULL;
+  if (workspace_bytes < static_cast<int64_t>(sizeof(AmaxWorkspace))) return BSQ_ERR_SHAPE;
+  if (!aligned(out, 4) || !aligned(workspace, 16) || (M > 0 && K > 0 && (!aligned(in, 16) || ld_in % 8 != 0)))
+    return BSQ_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AmaxWorkspace* ws = static_cast<AmaxWorkspace*>(workspace);
+  if (cudaMemsetAsync(&ws->counter, 0, sizeof(unsigned int), st) != cudaSuccess) return BSQ_ERR_CUDA;
+  const int64_t rows = (M > 0 && K > 0) ? M : 0;
+  int64_t grid = ceil_div(rows, kAmaxWarps);
+  const int64_t cap = std::min<int64_t>(kAmaxMaxBlocks, static_cast<int64_t>(d->sm_count) * 4);
+  grid = std::max<int64_t>(1, std::min(grid, cap));
+  const cudaError_t e = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(grid)),
+                                   dim3(kAmaxThreads), 0, st, static_cast<const uint16_t*>(in), rows,
+                                   static_cast<int>(K), ld_in, ws, out);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+int64_t bsq_grouped_tensor_sf_workspace_bytes(int32_t num_experts) {
+  if (num_experts < 1) return 0;
+  return 16 + ceil_div(static_cast<int64_t>(num_experts) * 4, 16) * 16;
+}
+
+int32_t bsq_grouped_tensor_sf(const void* in, int64_t in_rows, int64_t K, int64_t ld_in,
+                              const uint32_t* row_offsets, const int32_t* expert_ids,
+                              const int32_t* row_indices, int32_t G, int64_t total_rows,
+                              float* sf_out, int32_t num_experts, void* workspace,
+                              int64_t workspace_bytes, void* stream) {
+  if (num_experts < 1 || G < 0 || G > (1 << 20)) return BSQ_ERR_VALUE;
+  if (in_rows < 0 || K < 0 || K % 8 != 0 || K >= (int64_t(1) << 31) || total_rows < 0)
+    return BSQ_ERR_SHAPE;
+  if (K > 0 && ld_in < K) return BSQ_ERR_SHAPE;
+  if (workspace_bytes < bsq_grouped_tensor_sf_workspace_bytes(num_experts)) return BSQ_ERR_SHAPE;
+  if (!sf_out || !workspace || (G > 0 && (!row_offsets || !expert_ids || (K > 0 && !in))))
+    return BSQ_ERR_NULL;
+  if (!aligned(sf_out, 4) || !aligned(workspace, 16) || !aligned(row_offsets, 4) ||
+      !aligned(expert_ids, 4) || !aligned(row_indices, 4) ||
+      (K > 0 && (!aligned(in, 16) || ld_in % 8 != 0)))
+    return BSQ_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int* counter = static_cast<unsigned int*>(workspace);
+  unsigned int* amax_bits = counter + 4;
+  if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(bsq_grouped_tensor_sf_workspace_bytes(num_experts)), st) != cudaSuccess)
+    return BSQ_ERR_CUDA;
+  GroupedAmaxArgs a;
+  a.in = static_cast<const uint16_t*>(in);
+  a.ld_in = ld_in;
+  a.in_rows = in_rows;
+  a.K = static_cast<int>(K);
+  a.row_offsets = row_offsets;
+  a.expert_ids = expert_ids;
+  a.row_indices = row_indices;
+  a.G = G;
+  a.total_rows = (G > 0 && K > 0) ? total_rows : 0;
+  a.num_experts = num_experts;
+  a.amax_bits = amax_bits;
+  a.counter = counter;
+  a.sf = sf_out;
+  int64_t grid = ceil_div(a.total_rows, kAmaxWarps);
+  const int64_t cap = static_cast<int64_t>(d->sm_count) * 4;
+  grid = std::max<int64_t>(1, std::min(grid, cap));
+  const cudaError_t e = launch_pdl(grouped_amax_kernel, dim3(static_cast<unsigned>(grid)),
+                                   dim3(kAmaxThreads), 0, st, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
 int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows, int64_t K,

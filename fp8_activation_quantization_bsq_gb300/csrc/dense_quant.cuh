@@ -49,6 +49,7 @@ struct DenseArgs {
   int kt_atoms;        // 5D atoms per 128-row band: ceil(K / SF / 4)
   int vec32;           // packed rows allow 32-byte stores
   float tsf;
+  const float* tsf_dev;  // NVFP4: tensor_sf read from device memory (or null: use tsf)
 };
 
 template <int FMT, int STAGES>
@@ -115,8 +116,20 @@ __global__ void __launch_bounds__(kDenseThreads)
   // -------------------------------------------------------------- consumers
   // NVFP4 scale tables, filled while the first tiles are in flight; named
   // barrier 1 synchronizes the consumer warps only.
+  float tsf = a.tsf;
+  bool store_ok = true;
   if constexpr (FMT == kNVFP4) {
-    fill_nvfp4_factor_table(factor_tab, a.tsf, threadIdx.x, 32 * kDenseConsumerWarps);
+    if (a.tsf_dev != nullptr) {
+      // written by an earlier kernel in the stream: wait for it, read past L1
+      pdl_wait();
+      tsf = __ldcg(a.tsf_dev);
+      if (!(tsf > 0.0f && tsf <= 3.4028234663852886e38f)) {
+        if (threadIdx.x == 0) record_error(kErrValue);
+        store_ok = false;
+        tsf = 1.0f;
+      }
+    }
+    fill_nvfp4_factor_table(factor_tab, tsf, threadIdx.x, 32 * kDenseConsumerWarps);
     fill_div6_table(div6_tab, threadIdx.x, 32 * kDenseConsumerWarps);
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kDenseConsumerWarps) : "memory");
   }
@@ -129,7 +142,7 @@ __global__ void __launch_bounds__(kDenseThreads)
   const int r4 = lane >> 3;
   const int row = r32 + 32 * r4;
   const int atom_off = r32 * 16 + r4 * 4;  // this row's word inside a 512-byte atom
-  const NvScale ns{a.tsf, factor_tab, nullptr, div6_tab};
+  const NvScale ns{tsf, factor_tab, nullptr, div6_tab};
 
   int stage = 0;
   uint32_t phase = 0;
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(kDenseThreads)
     const int64_t grow = static_cast<int64_t>(mt) * kDenseTileRows + row;
     uint32_t sbytes = 0;
     if (valid) {
-      uint8_t* dst = grow < a.M ? a.out + grow * a.out_ld +
+      uint8_t* dst = grow < a.M && store_ok ? a.out + grow * a.out_ld +
                                       (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0)
                                 : nullptr;
       sbytes = quant_box_row<FMT, true>(smem + stage * kDenseStageBytes + h * kDenseBoxBytes + row * 128,
@@ -154,7 +167,9 @@ __global__ void __launch_bounds__(kDenseThreads)
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
 
     uint8_t* band = a.scales + static_cast<int64_t>(mt) * a.kt_atoms * 512 + atom_off;
-    if constexpr (FMT == kNVFP4) {
+    if (!store_ok) {
+      // invalid device tensor_sf: nothing is written
+    } else if constexpr (FMT == kNVFP4) {
       // one atom (64 columns) per box
       if (valid) *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
     } else {

@@ -1,0 +1,160 @@
+// NVFP4 tensor scales on the GPU: tensor_sf = fl32(448 * 6 / amax), amax the
+// exact max |x| of a BF16 tensor (or, per expert, over the expert's gathered
+// rows), 1.0 for an all-zero tensor.  These are the FP32 tensor_sf / per-expert
+// sf_tensor inputs of the NVFP4 quantize kernels, computed where the data is.
+//
+// Dense: warps stride over rows, lanes over 16-byte chunks (four loads in
+// flight per lane), max.xorsign.abs BF16 pairs, warp and block reductions;
+// every block stores its partial max in the workspace, and the last block to
+// finish (fenced atomic counter) reduces the partials and writes
+// {amax, tensor_sf}.  Grouped: one warp per destination row, its group by a
+// binary search over row_offsets, an atomic max per expert (non-negative FP32
+// maxima order like their bit patterns), and the last block writes sf_tensor.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace bsq {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxWarps = kAmaxThreads / 32;
+constexpr int kAmaxMaxBlocks = 1024;
+
+// Dense workspace: a completion counter and one partial per block.
+struct AmaxWorkspace {
+  unsigned int counter;
+  unsigned int pad[3];
+  unsigned int partial[kAmaxMaxBlocks];
+};
+
+__device__ __forceinline__ float tensor_sf_of(float amax) {
+  return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
+}
+
+// max |x| over one row of K BF16 elements (K % 8 == 0), as two BF16 halves.
+__device__ __forceinline__ uint32_t row_absmax(const uint16_t* row, int K, int lane) {
+  uint32_t acc = 0;
+  const int chunks = K >> 3;
+  int c = lane;
+  for (; c + 96 < chunks; c += 128) {
+    const uint4 v0 = ld_global_nc_v4(row + 8 * c), v1 = ld_global_nc_v4(row + 8 * (c + 32));
+    const uint4 v2 = ld_global_nc_v4(row + 8 * (c + 64)), v3 = ld_global_nc_v4(row + 8 * (c + 96));
+    acc = absmax2(acc, v0.x); acc = absmax2(acc, v0.y); acc = absmax2(acc, v0.z); acc = absmax2(acc, v0.w);
+    acc = absmax2(acc, v1.x); acc = absmax2(acc, v1.y); acc = absmax2(acc, v1.z); acc = absmax2(acc, v1.w);
+    acc = absmax2(acc, v2.x); acc = absmax2(acc, v2.y); acc = absmax2(acc, v2.z); acc = absmax2(acc, v2.w);
+    acc = absmax2(acc, v3.x); acc = absmax2(acc, v3.y); acc = absmax2(acc, v3.z); acc = absmax2(acc, v3.w);
+  }
+  for (; c < chunks; c += 32) {
+    const uint4 v = ld_global_nc_v4(row + 8 * c);
+    acc = absmax2(acc, v.x); acc = absmax2(acc, v.y); acc = absmax2(acc, v.z); acc = absmax2(acc, v.w);
+  }
+  return acc;
+}
+
+// Warp max of non-negative FP32 values, on their bit patterns.
+__device__ __forceinline__ uint32_t warp_max_bits(uint32_t b) {
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, x));
+  return b;
+}
+
+__global__ void __launch_bounds__(kAmaxThreads)
+    tensor_amax_kernel(const uint16_t* __restrict__ in, int64_t M, int K, int64_t ld,
+                       AmaxWorkspace* ws, float* out) {
+  __shared__ uint32_t warp_max[kAmaxWarps];
+  __shared__ bool last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  uint32_t acc = 0;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kAmaxWarps + warp; r < M;
+       r += static_cast<int64_t>(gridDim.x) * kAmaxWarps)
+    acc = absmax2(acc, row_absmax(in + r * ld, K, lane));
+  const uint32_t wm = warp_max_bits(__float_as_uint(absmax_final(acc)));
+  if (lane == 0) warp_max[warp] = wm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t bm = 0;
+    for (int w = 0; w < kAmaxWarps; ++w) bm = max(bm, warp_max[w]);
+    ws->partial[blockIdx.x] = bm;
+    __threadfence();
+    last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  // last block: reduce every block's partial
+  __threadfence();
+  uint32_t bm = 0;
+  for (int b = threadIdx.x; b < static_cast<int>(gridDim.x); b += kAmaxThreads)
+    bm = max(bm, __ldcg(ws->partial + b));
+  bm = warp_max_bits(bm);
+  if (lane == 0) warp_max[warp] = bm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < kAmaxWarps; ++w) m = max(m, warp_max[w]);
+    const float amax = __uint_as_float(m);
+    out[0] = amax;
+    out[1] = tensor_sf_of(amax);
+    ws->counter = 0;
+  }
+}
+
+struct GroupedAmaxArgs {
+  const uint16_t* in;
+  int64_t ld_in, in_rows;
+  int K;
+  const uint32_t* row_offsets;
+  const int32_t* expert_ids;
+  const int32_t* row_indices;  // may be null
+  int G;
+  int64_t total_rows;
+  int num_experts;
+  unsigned int* amax_bits;     // workspace: num_experts maxima (zeroed before launch)
+  unsigned int* counter;       // workspace: completion counter (zeroed before launch)
+  float* sf;                   // out: num_experts tensor scales
+};
+
+__global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const GroupedAmaxArgs a) {
+  __shared__ bool last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  const int64_t ro_end = a.G > 0 ? static_cast<int64_t>(__ldg(a.row_offsets + a.G)) : 0;  // no groups: no rows
+  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  for (int64_t d = static_cast<int64_t>(blockIdx.x) * kAmaxWarps + warp; d < rows;
+       d += static_cast<int64_t>(gridDim.x) * kAmaxWarps) {
+    int e = -1;
+    int64_t src = -1;
+    if (lane == 0) {
+      int lo = 0, hi = a.G - 1;  // g = max{g : ro[g] <= d}
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(a.row_offsets + mid + 1)) <= d) lo = mid + 1;
+        else hi = mid;
+      }
+      e = __ldg(a.expert_ids + lo);
+      src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
+      if (d < static_cast<int64_t>(__ldg(a.row_offsets + lo)) || e >= a.num_experts ||
+          (e >= 0 && (src < 0 || src >= a.in_rows))) {
+        record_error(kErrValue);
+        e = -1;
+      }
+    }
+    e = __shfl_sync(0xFFFFFFFFu, e, 0);
+    src = __shfl_sync(0xFFFFFFFFu, src, 0);
+    if (e < 0) continue;  // warp-uniform
+    const uint32_t m = warp_max_bits(__float_as_uint(absmax_final(row_absmax(a.in + src * a.ld_in, a.K, lane))));
+    if (lane == 0 && m != 0u) atomicMax(a.amax_bits + e, m);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < a.num_experts; e += kAmaxThreads)
+    a.sf[e] = tensor_sf_of(__uint_as_float(__ldcg(a.amax_bits + e)));
+}
+
+}  // namespace bsq

@@ -197,6 +197,56 @@ BSQ_API int32_t bsq_scales_interleave(const void* scales2d_dev, int64_t M, int64
                               void* scales5d_dev, void* stream);
 
 /*
+ * Dense quantize with the NVFP4 tensor_sf read from device memory
+ * (tensor_sf_dev: one float, e.g. element 1 of bsq_tensor_sf's output), so that
+ * computing the scale and quantizing chain on the GPU without a host round
+ * trip.  Same arguments and layouts as bsq_quantize otherwise; ignored for MX.
+ * A tensor_sf that is not finite and > 0 records BSQ_ERR_VALUE in the device
+ * error word and nothing is written.
+ */
+BSQ_API int32_t bsq_quantize_dynamic(int32_t fmt, const void* in_dev, int64_t M, int64_t K,
+                                     int64_t ld_in, void* out_dev, void* scales5d_dev,
+                                     const float* tensor_sf_dev, void* stream);
+
+/*
+ * NVFP4 per-tensor scale of a BF16 matrix, on the GPU:
+ *   amax = max |x| (exact), tensor_sf = fl32(448 * 6 / amax), 1.0 when amax == 0
+ *   (+Inf when amax < 2688 / FLT_MAX).
+ * (the FP32 tensor_sf of quantize_dynamic_scaled_async_fp4_kernel)
+ *   in_dev        BF16, M rows of K elements (K % 8 == 0), row stride ld_in
+ *                 elements (multiple of 8), 16-byte aligned.  M == 0 or K == 0:
+ *                 amax 0, tensor_sf 1.
+ *   out_dev       float[2] = {amax, tensor_sf} (device).
+ *   workspace_dev bsq_tensor_sf_workspace_bytes() bytes of caller-allocated
+ *                 device scratch, 16-byte aligned; its contents need no
+ *                 initialisation (the call resets what it uses).  Calls sharing
+ *                 one workspace must not overlap on the GPU.
+ */
+BSQ_API int64_t bsq_tensor_sf_workspace_bytes(void);
+BSQ_API int32_t bsq_tensor_sf(const void* in_dev, int64_t M, int64_t K, int64_t ld_in,
+                              float* out_dev, void* workspace_dev, int64_t workspace_bytes,
+                              void* stream);
+
+/*
+ * Per-expert NVFP4 scales of grouped activations, on the GPU: for every
+ * expert e, amax_e = max |x| over the source rows of the groups with
+ * expert_ids[g] == e (row_indices gather as in bsq_grouped_quantize),
+ * sf_dev[e] = fl32(448 * 6 / amax_e), or 1.0 when the expert has no rows.
+ * (the per-expert sf_tensor of grouped_quantize_dynamic_scaled_fp4_async_kernel)
+ *   num_experts   length of sf_dev (>= 1); expert ids >= num_experts or rows
+ *                 outside [0, in_rows) record BSQ_ERR_VALUE and are skipped.
+ *   workspace_dev bsq_grouped_tensor_sf_workspace_bytes(num_experts) bytes of
+ *                 device scratch, 16-byte aligned (zeroed by the call itself).
+ */
+BSQ_API int64_t bsq_grouped_tensor_sf_workspace_bytes(int32_t num_experts);
+BSQ_API int32_t bsq_grouped_tensor_sf(const void* in_dev, int64_t in_rows, int64_t K,
+                                      int64_t ld_in, const uint32_t* row_offsets_dev,
+                                      const int32_t* expert_ids_dev,
+                                      const int32_t* row_indices_dev, int32_t G,
+                                      int64_t total_rows, float* sf_dev, int32_t num_experts,
+                                      void* workspace_dev, int64_t workspace_bytes, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *code_out receives BSQ_OK or the first device-side error recorded since the
  * last call (BSQ_ERR_VALUE, BSQ_ERR_TIMEOUT).  Returns BSQ_ERR_CUDA if the

@@ -161,3 +161,44 @@ def test_grouped_kernel_choice_validation(lib):
     assert call(3) == VALUE and call(-1) == VALUE
     for k in (0, 1, 2):
         assert call(k, out=None) == NULL      # valid choice: stops at the next check
+
+
+def test_tensor_scale_validation(lib):
+    ws = lib.bsq_tensor_sf_workspace_bytes()
+    assert ws >= 16 + 4 * 1024
+    f = lib.bsq_tensor_sf
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    assert f(P, 4, 12, 12, P, P, ws, None) == SHAPE          # K % 8
+    assert f(P, -1, 16, 16, P, P, ws, None) == SHAPE
+    assert f(P, 4, 16, 8, P, P, ws, None) == SHAPE           # ld < K
+    assert f(P, 4, 16, 16, P, P, ws - 1, None) == SHAPE      # workspace too small
+    assert f(None, 4, 16, 16, P, P, ws, None) == NULL
+    assert f(P, 4, 16, 16, None, P, ws, None) == NULL
+    assert f(P, 4, 16, 16, P, None, ws, None) == NULL
+    assert f(P + 8, 4, 16, 16, P, P, ws, None) == ALIGN
+    assert f(P, 4, 16, 16, P + 2, P, ws, None) == ALIGN
+    assert f(P, 4, 16, 16, P, P + 4, ws, None) == ALIGN
+    g = lib.bsq_grouped_tensor_sf
+    g.restype = ctypes.c_int32
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    gws = lib.bsq_grouped_tensor_sf_workspace_bytes(8)
+    assert gws == 16 + 32 and lib.bsq_grouped_tensor_sf_workspace_bytes(0) == 0
+    assert g(P, 64, 256, 256, P, P, None, 4, 64, P, 0, P, gws, None) == VALUE
+    assert g(P, 64, 256, 256, P, P, None, -1, 64, P, 8, P, gws, None) == VALUE
+    assert g(P, 64, 100, 100, P, P, None, 4, 64, P, 8, P, gws, None) == SHAPE
+    assert g(P, 64, 256, 256, P, P, None, 4, 64, P, 8, P, gws - 1, None) == SHAPE
+    assert g(P, 64, 256, 256, None, P, None, 4, 64, P, 8, P, gws, None) == NULL
+    assert g(P, 64, 256, 256, P, P, None, 4, 64, None, 8, P, gws, None) == NULL
+    assert g(P, 64, 256, 256, P, P, P + 1, 4, 64, P, 8, P, gws, None) == ALIGN
+    q = lib.bsq_quantize_dynamic
+    q.restype = ctypes.c_int32
+    q.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert q(0, P, 128, 256, 256, P, P, None, None) == NULL      # NVFP4 needs the scale
+    assert q(0, P, 128, 256, 256, P, P, P + 2, None) == ALIGN
+    assert q(1, P, 128, 48, 48, P, P, None, None) == SHAPE
+    assert q(0, P, 0, 256, 256, None, None, None, None) == OK     # empty: no-op

@@ -1,0 +1,137 @@
+"""GPU parity of the tensor-scale reductions (global and per-expert amax ->
+NVFP4 tensor_sf) and of quantize_dynamic, which reads tensor_sf from device
+memory, against the CPU oracle: amax and tensor_sf bit-exact, packed bytes
+and scales bit-exact."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from bsq_testlib import SENTINEL, guarded, i32_device, margin_intact, to_device_bf16, u32_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    import fp8_activation_quantization_bsq_gb300 as m
+    from fp8_activation_quantization_bsq_gb300 import _build
+    _build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _f32(t):
+    return t.cpu().numpy().astype(np.float32)
+
+
+CASES = {
+    "small": lambda: wl.config_dense_nvfp4_small()["x_bits"],
+    "large": lambda: wl.config_dense_nvfp4_large()["x_bits"],
+    "zeros": lambda: np.zeros((70, 64), np.uint16),
+    "neg_zero_and_max": lambda: np.array([[0x8000, 0xFF7F] + [0] * 14], np.uint16),
+    "one_row": lambda: wl.dense_activations(np.random.Generator(np.random.PCG64(1)), 1, 8, "normal"),
+    "many_rows": lambda: wl.dense_activations(np.random.Generator(np.random.PCG64(2)), 40000, 16, "rowlognormal"),
+    "subnormal_max": lambda: np.array([[0x0003, 0x8001] * 8], np.uint16),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_tensor_sf_exact(bsq, case):
+    bits = CASES[case]()
+    x = to_device_bf16(bits)
+    out = bsq.tensor_sf(x)
+    amax, tsf = oracle.tensor_sf(bits)
+    got = _f32(out)
+    assert got[0] == amax
+    assert got[1] == tsf or (np.isinf(tsf) and np.isinf(got[1]))
+    assert bsq.device_error() == 0
+
+
+def test_tensor_sf_strided_and_workspace_reuse(bsq):
+    rng = np.random.Generator(np.random.PCG64(3))
+    bits = wl.dense_activations(rng, 300, 96, "rowlognormal")
+    wide = np.zeros((300, 136), np.uint16)
+    wide[:, :96] = bits
+    wide[:, 96:] = 0x7F00                            # huge values outside the view
+    x = to_device_bf16(wide)[:, :96]
+    ws = torch.empty(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    for _ in range(3):                               # the workspace is reused as is
+        out = bsq.tensor_sf(x, workspace=ws)
+        amax, tsf = oracle.tensor_sf(bits)
+        assert _f32(out)[0] == amax and _f32(out)[1] == tsf
+    empty = torch.empty((0, 32), dtype=torch.bfloat16, device="cuda")
+    np.testing.assert_array_equal(_f32(bsq.tensor_sf(empty, workspace=ws)), [0.0, 1.0])
+
+
+@pytest.mark.parametrize("cfg", ["prefill_small", "decode", "negative_ids"])
+def test_grouped_tensor_sf_exact(bsq, cfg):
+    if cfg == "decode":
+        d = wl.config_grouped_decode(K=2048)
+        E = 256
+    else:
+        d = wl.config_grouped_prefill(seed=5, tokens=200, K=256, num_experts=32, top_k=4)
+        E = 32
+    eid = d["expert_ids"].copy()
+    if cfg == "negative_ids":
+        eid[::4] = -1
+    x = to_device_bf16(d["x_bits"])
+    sf = bsq.grouped_tensor_sf(x, u32_device(d["row_offsets"]), i32_device(eid), E,
+                               i32_device(d["row_indices"]), total_rows=d["total_rows"])
+    amax, ref = oracle.expert_tensor_sf(d["x_bits"], d["row_offsets"], eid, E, d["row_indices"])
+    np.testing.assert_array_equal(_f32(sf), ref)
+    assert bsq.device_error() == 0
+
+
+def test_grouped_tensor_sf_no_groups_gives_ones(bsq):
+    x = torch.zeros((4, 32), dtype=torch.bfloat16, device="cuda")
+    sf = bsq.grouped_tensor_sf(x, u32_device(np.zeros(1, np.uint32)),
+                               i32_device(np.zeros(0, np.int32)), 5, total_rows=0)
+    np.testing.assert_array_equal(_f32(sf), np.ones(5, np.float32))
+
+
+@pytest.mark.parametrize("case", ["small", "large"])
+def test_quantize_dynamic_chain_matches_oracle(bsq, case):
+    """tensor_sf then quantize_dynamic on one stream, no host round trip."""
+    bits = CASES[case]()
+    M, K = bits.shape
+    x = to_device_bf16(bits)
+    packed, scales = bsq.quantize_dynamic(x, "nvfp4")
+    _, tsf = oracle.tensor_sf(bits)
+    if case == "large":
+        rows = np.arange(0, M, 97)
+        p_ref, s_ref = oracle.quantize_rank2("nvfp4", bits[rows], tsf)
+        np.testing.assert_array_equal(packed.cpu().numpy()[rows], p_ref)
+        S = K // 16
+        mm, ss = np.meshgrid(rows, np.arange(S), indexing="ij")
+        np.testing.assert_array_equal(scales.cpu().numpy()[oracle.offset_5d(mm, ss, -(-S // 4))], s_ref)
+    else:
+        p_ref, s_ref = oracle.quantize("nvfp4", bits, tsf)
+        np.testing.assert_array_equal(packed.cpu().numpy(), p_ref)
+        np.testing.assert_array_equal(scales.cpu().numpy(), s_ref)
+    assert bsq.device_error() == 0
+
+
+@pytest.mark.parametrize("bad", [0.0, -1.0, float("nan"), float("inf")])
+def test_quantize_dynamic_rejects_bad_device_scale(bsq, bad):
+    bits = CASES["small"]()
+    x = to_device_bf16(bits)
+    M, K = bits.shape
+    ofull, out = guarded(M * K // 2)
+    sfull, sc = guarded(oracle.scales5d_bytes(M, K // 16))
+    tsf = torch.tensor([bad], dtype=torch.float32, device="cuda")
+    bsq.quantize_dynamic(x, "nvfp4", tsf, out=out, scales=sc)
+    assert bsq.device_error() == 4
+    assert np.all(ofull.cpu().numpy() == SENTINEL) and np.all(sfull.cpu().numpy() == SENTINEL)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+def test_quantize_dynamic_mx_ignores_scale(bsq, fmt):
+    bits = CASES["small"]()
+    x = to_device_bf16(bits)
+    packed, scales = bsq.quantize_dynamic(x, fmt, None)
+    p_ref, s_ref = oracle.quantize(fmt, bits)
+    np.testing.assert_array_equal(packed.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(scales.cpu().numpy(), s_ref)
