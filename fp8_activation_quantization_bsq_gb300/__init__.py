@@ -49,6 +49,8 @@ _SIGNATURES = {
     "bsq_tensor_sf_workspace_bytes": (_c_i64, []),
     "bsq_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p]),
     "bsq_grouped_tensor_sf_workspace_bytes": (_c_i64, [_c_i32]),
+    "bsq_grouped_tensor_sf_noalloc": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i32,
+                                               _c_i64, _c_p, _c_i32, _c_p]),
     "bsq_grouped_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i32,
                                        _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p]),
     "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),

@@ -471,3 +471,97 @@ int32_t bsq_device_error(void* stream, int32_t* code_out) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Per-expert tensor scales without caller-provided scratch.
+//
+// Some callers have no way to obtain device memory at the point where they
+// need the scales: a plugin whose C interface passes only input and output
+// pointers, a host framework that owns every device allocation through its
+// own pool and forbids raw cudaMalloc, or a latency-critical loop that cannot
+// afford the device-wide synchronization cudaMalloc/cudaFree may imply.  For
+// them the reduction's scratch (a completion counter and one running maximum
+// per expert) lives in the file-scope array below, one copy per device that
+// loads this library, held until the process exits.  Host code must not use
+// the array's name as a device address: it is a host-side stand-in, and only
+// the address cudaGetSymbolAddress returns for the current device is valid.
+namespace {
+
+constexpr int kNoAllocScratchWords = 4 + BSQ_NOALLOC_MAX_EXPERTS;  // counter (+3 pad) | maxima
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchWords];
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned int* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sm_count = 0;
+};
+
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_devices[kMaxDevices];
+
+// Once per device, with that device current: look up the array's device
+// address and the SM count.
+bsq_status noalloc_device(NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_devices[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return BSQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BSQ_ERR_CUDA;
+    d.scratch = static_cast<unsigned int*>(ptr);
+    d.ready = true;
+  }
+  *out = &d;
+  return BSQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bsq_grouped_tensor_sf_noalloc(const void* in, int64_t in_rows, int64_t K, int64_t ld_in,
+                                      const uint32_t* row_offsets, const int32_t* expert_ids,
+                                      const int32_t* row_indices, int32_t G, int64_t total_rows,
+                                      float* sf_out, int32_t num_experts, void* stream) {
+  if (num_experts < 1 || G < 0 || G > (1 << 20)) return BSQ_ERR_VALUE;
+  if (num_experts > BSQ_NOALLOC_MAX_EXPERTS) return BSQ_ERR_SHAPE;  // beyond the static scratch
+  if (in_rows < 0 || K < 0 || K % 8 != 0 || K >= (int64_t(1) << 31) || total_rows < 0)
+    return BSQ_ERR_SHAPE;
+  if (K > 0 && ld_in < K) return BSQ_ERR_SHAPE;
+  if (!sf_out || (G > 0 && (!row_offsets || !expert_ids || (K > 0 && !in)))) return BSQ_ERR_NULL;
+  if (!aligned(sf_out, 4) || !aligned(row_offsets, 4) || !aligned(expert_ids, 4) ||
+      !aligned(row_indices, 4) || (K > 0 && (!aligned(in, 16) || ld_in % 8 != 0)))
+    return BSQ_ERR_ALIGN;
+  NoAllocDevice* d = nullptr;
+  if (bsq_status s = noalloc_device(&d); s != BSQ_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's counter and maxima: zero the part
+  // this call uses (counter, padding and num_experts maxima).
+  const size_t clear_bytes = static_cast<size_t>(16 + 4 * static_cast<int64_t>(num_experts));
+  if (cudaMemsetAsync(d->scratch, 0, clear_bytes, st) != cudaSuccess) return BSQ_ERR_CUDA;
+  GroupedAmaxArgs a;
+  a.in = static_cast<const uint16_t*>(in);
+  a.ld_in = ld_in;
+  a.in_rows = in_rows;
+  a.K = static_cast<int>(K);
+  a.row_offsets = row_offsets;
+  a.expert_ids = expert_ids;
+  a.row_indices = row_indices;
+  a.G = G;
+  a.total_rows = (G > 0 && K > 0) ? total_rows : 0;
+  a.num_experts = num_experts;
+  a.amax_bits = d->scratch + 4;
+  a.counter = d->scratch;
+  a.sf = sf_out;
+  int64_t grid = ceil_div(a.total_rows, kAmaxWarps);
+  grid = std::max<int64_t>(1, std::min<int64_t>(grid, static_cast<int64_t>(d->sm_count) * 4));
+  const cudaError_t e = launch_pdl(grouped_amax_kernel, dim3(static_cast<unsigned>(grid)),
+                                   dim3(kAmaxThreads), 0, st, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+}  // extern "C"

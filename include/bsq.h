@@ -247,6 +247,39 @@ BSQ_API int32_t bsq_grouped_tensor_sf(const void* in_dev, int64_t in_rows, int64
                                       void* workspace_dev, int64_t workspace_bytes, void* stream);
 
 /*
+ * bsq_grouped_tensor_sf without a workspace argument: the same per-expert
+ * scales, bit for bit, for callers that cannot allocate device memory where
+ * they need them -- a plugin whose C interface hands over only input and
+ * output buffers, a host framework that owns all device memory through its
+ * own pool and forbids direct cudaMalloc, or a latency-critical loop that
+ * cannot take the device-wide synchronization cudaMalloc/cudaFree may cause.
+ * The paper has no counterpart of this entry point; it is an addition of this
+ * library.
+ *   Scratch       a static device array inside this library (16 + 4 *
+ *                 BSQ_NOALLOC_MAX_EXPERTS bytes, one copy on every device that
+ *                 loads the library, kept until the process exits).  Nothing is
+ *                 allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   Limit         num_experts <= BSQ_NOALLOC_MAX_EXPERTS; larger returns
+ *                 BSQ_ERR_SHAPE before anything is enqueued.  num_experts < 1
+ *                 returns BSQ_ERR_VALUE.
+ *   First call    on a device looks up the array's device address and the SM
+ *                 count (cudaGetSymbolAddress, cudaDeviceGetAttribute) with that
+ *                 device current; make it before any stream capture begins.
+ *   Sharing       every call on a device uses the same array; each call clears
+ *                 the part it uses on `stream` first.  Calls that overlap on the
+ *                 GPU (other streams, other host threads, without ordering
+ *                 between them) race on the array and give wrong scales.
+ * Other arguments, layouts and device-side errors as bsq_grouped_tensor_sf.
+ */
+#define BSQ_NOALLOC_MAX_EXPERTS 1024
+BSQ_API int32_t bsq_grouped_tensor_sf_noalloc(const void* in_dev, int64_t in_rows, int64_t K,
+                                              int64_t ld_in, const uint32_t* row_offsets_dev,
+                                              const int32_t* expert_ids_dev,
+                                              const int32_t* row_indices_dev, int32_t G,
+                                              int64_t total_rows, float* sf_dev,
+                                              int32_t num_experts, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *code_out receives BSQ_OK or the first device-side error recorded since the
  * last call (BSQ_ERR_VALUE, BSQ_ERR_TIMEOUT).  Returns BSQ_ERR_CUDA if the
