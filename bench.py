@@ -89,7 +89,7 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-DENSE_SOURCES = ("device_common.cuh", "dense_quant.cuh")
+DENSE_SOURCES = ("device_common.cuh", "box_quant.cuh", "dense_quant.cuh")
 
 
 def source_digest() -> str:

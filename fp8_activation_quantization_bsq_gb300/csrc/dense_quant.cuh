@@ -56,8 +56,10 @@ template <int FMT, int STAGES>
 __global__ void __launch_bounds__(kDenseThreads)
     dense_quant_tma_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte alignment (128-byte swizzle atoms) by an offset from the shared
+  // array itself, so that every access below stays a shared-space load
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+  uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * kDenseStageBytes);
   uint64_t* empty_bar = full_bar + STAGES;
   float* factor_tab = reinterpret_cast<float*>(empty_bar + STAGES);
