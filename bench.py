@@ -239,7 +239,7 @@ def extra_workloads(bsq, device, flush, peak):
     x = to_dev_bf16(c["x_bits"], device)
     M, K = c["x_bits"].shape
     del c
-    ws = torch.empty(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
+    ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
     tsf = bsq.tensor_sf(x, workspace=ws)
     mean, mn = time_events(lambda: bsq.tensor_sf(x, out=tsf, workspace=ws), reps, flush)
     res[f"tensor_sf_M{M}_K{K}"] = {"us": round(mean * 1e3, 2), "GB_s": round(M * K * 2 / (mean * 1e6), 1),
@@ -298,7 +298,7 @@ def extra_workloads(bsq, device, flush, peak):
     eid = torch.from_numpy(d["expert_ids"]).to(device)
     ridx = torch.from_numpy(d["row_indices"]).to(device)
     E = d["num_experts"]
-    gws = torch.empty(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device=device)
+    gws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device=device)
     gsf = bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], workspace=gws)
     mean, mn = time_events(lambda: bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"],
                                                          out=gsf, workspace=gws), reps, flush)
@@ -539,6 +539,64 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+CASES = ("grouped_prefill", "grouped_decode", "tensor_sf", "grouped_tensor_sf", "mxfp8", "mxfp4")
+
+
+def run_case(args):
+    """One context workload alone (for profiling a single kernel): warm-up
+    launches, then ``--steps`` launches back to back on one GPU; prints one
+    JSON line with the mean microseconds per launch (CUDA events)."""
+    import torch
+    import fp8_activation_quantization_bsq_gb300 as bsq
+    import workloads as wl
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if args.case in ("grouped_prefill", "grouped_decode", "grouped_tensor_sf"):
+        d = wl.config_grouped_prefill() if args.case != "grouped_decode" else wl.config_grouped_decode()
+        x = to_dev_bf16(d["x_bits"], device)
+        u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
+        ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
+        eid = torch.from_numpy(d["expert_ids"]).to(device)
+        sf = torch.from_numpy(d["sf_tensor"]).to(device)
+        ridx = torch.from_numpy(d["row_indices"]).to(device)
+        kw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=8)
+        if args.case == "grouped_tensor_sf":
+            ws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(d["num_experts"]),
+                             dtype=torch.uint8, device=device)
+            out = bsq.grouped_tensor_sf(x, ro, eid, d["num_experts"], ridx, total_rows=d["total_rows"],
+                                        workspace=ws)
+            fn = lambda: bsq.grouped_tensor_sf(x, ro, eid, d["num_experts"], ridx, total_rows=d["total_rows"],
+                                               out=out, workspace=ws)
+        else:
+            out, sc = bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, **kw)
+            fn = lambda: bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
+    elif args.case == "tensor_sf":
+        x = to_dev_bf16(wl.config_dense_nvfp4_large()["x_bits"], device)
+        ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
+        out = bsq.tensor_sf(x, workspace=ws)
+        fn = lambda: bsq.tensor_sf(x, out=out, workspace=ws)
+    else:
+        x = to_dev_bf16(wl.config_dense_mx_wide()["x_bits"], device)
+        out, sc = bsq.quantize(x, args.case)
+        fn = lambda: bsq.quantize(x, args.case, out=out, scales=sc)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_hold(1.0 + 0.2 * args.steps)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    err = bsq.device_error()
+    print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
+                      "us_per_launch": round(a.elapsed_time(b) * 1e3 / args.steps, 2),
+                      "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -547,9 +605,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the context workloads")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="time one context workload alone on GPU 0 (for profiling) and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case is not None:
+        run_case(args)
+        return
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -159,13 +159,15 @@ def quantize_dynamic(x: torch.Tensor, fmt, tensor_sf_dev=None, out=None, scales=
 
 def tensor_sf(x: torch.Tensor, out=None, workspace=None, stream=None):
     """float32 CUDA tensor [amax, tensor_sf] of a 2-D BF16 CUDA tensor,
-    tensor_sf = fl32(448*6/amax) (1.0 for an all-zero tensor)."""
+    tensor_sf = fl32(448*6/amax) (1.0 for an all-zero tensor).  A reused
+    ``workspace`` must have been zeroed once (``torch.zeros``); each call
+    leaves it zeroed."""
     _check_x(x)
     M, K = x.shape
     if out is None:
         out = torch.empty(2, dtype=torch.float32, device=x.device)
     if workspace is None:
-        workspace = torch.empty(lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=x.device)
     with torch.cuda.device(x.device):
         rc = lib().bsq_tensor_sf(_ptr(x), M, K, x.stride(0) if M else K, _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(x.device, stream))
@@ -186,7 +188,7 @@ def grouped_tensor_sf(x: torch.Tensor, row_offsets, expert_ids, num_experts: int
     if out is None:
         out = torch.empty(num_experts, dtype=torch.float32, device=x.device)
     if workspace is None:
-        workspace = torch.empty(lib().bsq_grouped_tensor_sf_workspace_bytes(num_experts),
+        workspace = torch.zeros(lib().bsq_grouped_tensor_sf_workspace_bytes(num_experts),
                                 dtype=torch.uint8, device=x.device)
     with torch.cuda.device(x.device):
         rc = lib().bsq_grouped_tensor_sf(_ptr(x), in_rows, K, x.stride(0) if in_rows else K,

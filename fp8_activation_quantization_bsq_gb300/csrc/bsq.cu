@@ -301,7 +301,6 @@ int32_t bsq_tensor_sf(const void* in, int64_t M, int64_t K, int64_t ld_in, float
   if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   AmaxWorkspace* ws = static_cast<AmaxWorkspace*>(workspace);
-  if (cudaMemsetAsync(&ws->counter, 0, sizeof(unsigned int), st) != cudaSuccess) return BSQ_ERR_CUDA;
   const int64_t rows = (M > 0 && K > 0) ? M : 0;
   int64_t grid = ceil_div(rows, kAmaxWarps);
   const int64_t cap = std::min<int64_t>(kAmaxMaxBlocks, static_cast<int64_t>(d->sm_count) * 4);
@@ -338,8 +337,6 @@ int32_t bsq_grouped_tensor_sf(const void* in, int64_t in_rows, int64_t K, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned int* counter = static_cast<unsigned int*>(workspace);
   unsigned int* amax_bits = counter + 4;
-  if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(bsq_grouped_tensor_sf_workspace_bytes(num_experts)), st) != cudaSuccess)
-    return BSQ_ERR_CUDA;
   GroupedAmaxArgs a;
   a.in = static_cast<const uint16_t*>(in);
   a.ld_in = ld_in;

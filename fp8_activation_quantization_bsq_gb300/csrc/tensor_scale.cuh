@@ -10,6 +10,7 @@
 // {amax, tensor_sf}.  Grouped: one warp per destination row, its group by a
 // binary search over row_offsets, an atomic max per expert (non-negative FP32
 // maxima order like their bit patterns), and the last block writes sf_tensor.
+// Both leave their workspace zeroed for the next launch.
 #pragma once
 
 #include "device_common.cuh"
@@ -20,7 +21,11 @@ constexpr int kAmaxThreads = 256;
 constexpr int kAmaxWarps = kAmaxThreads / 32;
 constexpr int kAmaxMaxBlocks = 1024;
 
-// Dense workspace: a completion counter and one partial per block.
+// Dense workspace: a completion counter and one partial per block.  The
+// caller zeroes it once; the last block of every launch sets the counter
+// back to zero, so consecutive launches need no memset in between.  A
+// counter outside [0, gridDim.x) (a workspace never zeroed) records
+// BSQ_ERR_VALUE.
 struct AmaxWorkspace {
   unsigned int counter;
   unsigned int pad[3];
@@ -77,7 +82,9 @@ __global__ void __launch_bounds__(kAmaxThreads)
     for (int w = 0; w < kAmaxWarps; ++w) bm = max(bm, warp_max[w]);
     ws->partial[blockIdx.x] = bm;
     __threadfence();
-    last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+    const unsigned int ticket = atomicAdd(&ws->counter, 1u);
+    if (ticket >= gridDim.x) record_error(kErrValue);
+    last = ticket == gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
@@ -109,8 +116,8 @@ struct GroupedAmaxArgs {
   int G;
   int64_t total_rows;
   int num_experts;
-  unsigned int* amax_bits;     // workspace: num_experts maxima (zeroed before launch)
-  unsigned int* counter;       // workspace: completion counter (zeroed before launch)
+  unsigned int* amax_bits;     // workspace: num_experts maxima (zero at launch, zeroed again)
+  unsigned int* counter;       // workspace: completion counter (zero at launch, zeroed again)
   float* sf;                   // out: num_experts tensor scales
 };
 
@@ -148,13 +155,18 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+    const unsigned int ticket = atomicAdd(a.counter, 1u);
+    if (ticket >= gridDim.x) record_error(kErrValue);
+    last = ticket == gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int e = threadIdx.x; e < a.num_experts; e += kAmaxThreads)
+  for (int e = threadIdx.x; e < a.num_experts; e += kAmaxThreads) {
     a.sf[e] = tensor_sf_of(__uint_as_float(__ldcg(a.amax_bits + e)));
+    a.amax_bits[e] = 0u;  // ready for the next launch
+  }
+  if (threadIdx.x == 0) *a.counter = 0u;
 }
 
 }  // namespace bsq

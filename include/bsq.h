@@ -218,9 +218,12 @@ BSQ_API int32_t bsq_quantize_dynamic(int32_t fmt, const void* in_dev, int64_t M,
  *                 amax 0, tensor_sf 1.
  *   out_dev       float[2] = {amax, tensor_sf} (device).
  *   workspace_dev bsq_tensor_sf_workspace_bytes() bytes of caller-allocated
- *                 device scratch, 16-byte aligned; its contents need no
- *                 initialisation (the call resets what it uses).  Calls sharing
- *                 one workspace must not overlap on the GPU.
+ *                 device scratch, 16-byte aligned, zeroed by the caller once
+ *                 before its first use (e.g. cudaMemsetAsync); every call leaves
+ *                 it zeroed again, so consecutive calls need no memset.  A
+ *                 workspace that was not zeroed records BSQ_ERR_VALUE in the
+ *                 device error word (the outputs are then not written).  Calls
+ *                 sharing one workspace must not overlap on the GPU.
  */
 BSQ_API int64_t bsq_tensor_sf_workspace_bytes(void);
 BSQ_API int32_t bsq_tensor_sf(const void* in_dev, int64_t M, int64_t K, int64_t ld_in,
@@ -236,7 +239,11 @@ BSQ_API int32_t bsq_tensor_sf(const void* in_dev, int64_t M, int64_t K, int64_t 
  *   num_experts   length of sf_dev (>= 1); expert ids >= num_experts or rows
  *                 outside [0, in_rows) record BSQ_ERR_VALUE and are skipped.
  *   workspace_dev bsq_grouped_tensor_sf_workspace_bytes(num_experts) bytes of
- *                 device scratch, 16-byte aligned (zeroed by the call itself).
+ *                 device scratch, 16-byte aligned, zeroed by the caller once
+ *                 before its first use; every call leaves it zeroed again (as
+ *                 for bsq_tensor_sf; a workspace not zeroed records
+ *                 BSQ_ERR_VALUE).  Calls sharing one workspace must not overlap
+ *                 on the GPU.
  */
 BSQ_API int64_t bsq_grouped_tensor_sf_workspace_bytes(int32_t num_experts);
 BSQ_API int32_t bsq_grouped_tensor_sf(const void* in_dev, int64_t in_rows, int64_t K,

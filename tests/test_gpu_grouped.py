@@ -218,3 +218,21 @@ def test_grouped_offsets_beyond_buffers_are_reported(bsq, kernel):
                                              d["sf_tensor"], d["row_indices"])
     np.testing.assert_array_equal(p[:r0], p_ref[:r0])
     assert np.all(p[r0:] == SENTINEL)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("K", [256, 96])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_source_rows_with_many_copies(bsq, fmt, K, kernel):
+    """Source rows gathered into many destination rows: 40 and 17 copies of
+    two rows among ordinary top-2 routing, each copy quantized with its own
+    group's expert scale."""
+    d = wl.config_grouped_prefill(seed=9, tokens=70, K=K, num_experts=24, top_k=2)
+    ridx = d["row_indices"].copy()
+    rng = np.random.Generator(np.random.PCG64(9))
+    pos = rng.permutation(len(ridx))
+    ridx[pos[:40]] = 5
+    ridx[pos[40:57]] = 37
+    d = dict(d, row_indices=ridx)
+    p, s = _run_grouped(bsq, fmt, d, 1, kernel=kernel)
+    _compare(fmt, d, p, s)

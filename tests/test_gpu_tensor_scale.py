@@ -57,7 +57,7 @@ def test_tensor_sf_strided_and_workspace_reuse(bsq):
     wide[:, :96] = bits
     wide[:, 96:] = 0x7F00                            # huge values outside the view
     x = to_device_bf16(wide)[:, :96]
-    ws = torch.empty(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device="cuda")
     for _ in range(3):                               # the workspace is reused as is
         out = bsq.tensor_sf(x, workspace=ws)
         amax, tsf = oracle.tensor_sf(bits)
@@ -135,3 +135,28 @@ def test_quantize_dynamic_mx_ignores_scale(bsq, fmt):
     p_ref, s_ref = oracle.quantize(fmt, bits)
     np.testing.assert_array_equal(packed.cpu().numpy(), p_ref)
     np.testing.assert_array_equal(scales.cpu().numpy(), s_ref)
+
+
+def test_workspaces_left_zeroed_and_unzeroed_ones_reported(bsq):
+    """Each call leaves its workspace zeroed for the next one; a workspace
+    that was never zeroed is reported (BSQ_ERR_VALUE), not silently used."""
+    bits = CASES["small"]()
+    x = to_device_bf16(bits)
+    ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bsq.tensor_sf(x, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    d = wl.config_grouped_prefill(seed=5, tokens=200, K=256, num_experts=32, top_k=4)
+    gws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(32), dtype=torch.uint8, device="cuda")
+    args = (to_device_bf16(d["x_bits"]), u32_device(d["row_offsets"]), i32_device(d["expert_ids"]), 32,
+            i32_device(d["row_indices"]))
+    bsq.grouped_tensor_sf(*args, total_rows=d["total_rows"], workspace=gws)
+    torch.cuda.synchronize()
+    assert int(gws.count_nonzero().item()) == 0
+    assert bsq.device_error() == 0
+    bad = torch.full_like(ws, 0xFF)
+    bsq.tensor_sf(x, workspace=bad)
+    assert bsq.device_error() == 4
+    gbad = torch.full_like(gws, 0xFF)
+    bsq.grouped_tensor_sf(*args, total_rows=d["total_rows"], workspace=gbad)
+    assert bsq.device_error() == 4

@@ -65,7 +65,7 @@ def _noalloc(lib, c, num_experts=None):
 def _with_workspace(lib, c):
     E = c["E"]
     sf = torch.full((E,), -1.0, dtype=torch.float32, device="cuda")
-    ws = torch.empty(lib.bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(lib.bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device="cuda")
     x = c["x"]
     rc = lib.bsq_grouped_tensor_sf(_p(x), x.shape[0], x.shape[1], x.stride(0), _p(c["ro"]), _p(c["eid"]),
                                    _p(c["ridx"]), c["G"], c["total_rows"], _p(sf), E, _p(ws), ws.numel(),
