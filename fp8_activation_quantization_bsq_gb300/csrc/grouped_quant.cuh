@@ -13,10 +13,10 @@
 //    the last round also reads row_offsets and expert_ids at the probe
 //    positions, so up to 256 groups cost one round of loads).  Then, as in
 //    the dense kernel, each lane owns one row and one 64-column half of a
-//    tile.  Each warp streams its 32 rows' gathered segments into a 3-deep
+//    tile.  Each warp streams its 32 rows' gathered segments into a 2-deep
 //    shared-memory ring with cp.async (8 lanes per row, so each instruction
-//    moves 4 rows x 128 B in whole sectors; two column tiles in flight while
-//    the third is quantized; the warp waits only for its own copy groups, so
+//    moves 4 rows x 128 B in whole sectors; one column tile in flight while
+//    the other is quantized, three blocks per SM; the warp waits only for its own copy groups, so
 //    the loop has no block barrier), then each lane quantizes its row from
 //    shared memory with the block's element-scale table and stores whole
 //    sectors.  Warps own 32 consecutive rows, so the unused rows of a
@@ -158,7 +158,12 @@ constexpr int kGtWarps = 8;
 constexpr int kGtThreads = 32 * kGtWarps;
 constexpr int kGtPitch = 272;                     // bytes per staged row: 2 x 128 + 16 pad
 constexpr int kGtStageBytes = 128 * kGtPitch;
-constexpr int kGtStages = 3;
+// Two stages (one column tile in flight while one is quantized) and three
+// resident blocks per SM: 24 warps per SM hide the gather and arithmetic
+// latency better than three stages at two blocks per SM (shared memory
+// limits residency to 2 blocks at 3 stages).
+constexpr int kGtStages = 2;                      // 1 to 3
+constexpr int kGtMinBlocks = 3;                   // resident blocks per SM (launch bounds)
 constexpr int kGtSmemBytes = kGtStages * kGtStageBytes;
 
 struct GtShared {
@@ -179,8 +184,23 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// A warp's gathered copies of one 64-column half of a column tile: in copy k
+// (0..7) lane l moves 16-byte chunk cc = l % 8 of tile row crow0 + 4k (crow0 =
+// the warp's first row + l / 8) from source row csrc[k] (skipped when < 0).
+// One commit group per call, empty beyond K, keeps wait_group counts exact.
+__device__ __forceinline__ void gt_issue(const GroupedArgs& a, uint8_t* stage_half, int col0, int cc,
+                                         int crow0, const int64_t (&csrc)[8]) {
+  if (col0 < a.K && cc < (a.K - col0) / 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (csrc[k] >= 0)
+        cp_async16(stage_half + (crow0 + 4 * k) * kGtPitch + 16 * cc, a.in + csrc[k] * a.ld_in + col0 + 8 * cc);
+  }
+  cp_async_commit();
+}
+
 template <int FMT>
-__global__ void __launch_bounds__(kGtThreads, 2) grouped_tile_kernel(const GroupedArgs a) {
+__global__ void __launch_bounds__(kGtThreads, kGtMinBlocks) grouped_tile_kernel(const GroupedArgs a) {
   __shared__ GtShared sh;
   extern __shared__ __align__(128) uint8_t ring[];
   const int warp = threadIdx.x >> 5;
@@ -242,25 +262,18 @@ __global__ void __launch_bounds__(kGtThreads, 2) grouped_tile_kernel(const Group
 
   const int kt_beg = blockIdx.y * a.ktc;
   const int kt_end = min(a.tiles_k, kt_beg + a.ktc);
-  // one copy group per column tile (empty beyond K) keeps wait_group exact
   auto issue = [&](int kt) {
-    const int col0 = kt * 128 + 64 * h;
-    if (col0 < a.K && cc < (a.K - col0) / 8) {
-      uint8_t* stage = ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + h * 128 + 16 * cc;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int crow = wr + (lane >> 3) + 4 * k;
-        if (csrc[k] >= 0) cp_async16(stage + crow * kGtPitch, a.in + csrc[k] * a.ld_in + col0 + 8 * cc);
-      }
-    }
-    cp_async_commit();
+    gt_issue(a, ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + h * 128, kt * 128 + 64 * h, cc,
+             wr + (lane >> 3), csrc);
   };
-  issue(kt_beg);
-  if (kt_beg + 1 < kt_end) issue(kt_beg + 1);
+  constexpr int kAhead = kGtStages - 1;        // column tiles in flight while one is quantized
+#pragma unroll
+  for (int i = 0; i < kAhead; ++i)
+    if (kt_beg + i < kt_end) issue(kt_beg + i);
 #pragma unroll 1
   for (int kt = kt_beg; kt < kt_end; ++kt) {
-    const int ahead = min(2, kt_end - 1 - kt);  // groups committed after tile kt
-    if (kt + 2 < kt_end) issue(kt + 2);         // into the slot freed two tiles ago
+    const int ahead = min(kAhead, kt_end - 1 - kt);  // groups committed after tile kt
+    if (kt + kAhead < kt_end) issue(kt + kAhead);     // into the slot freed kAhead tiles ago
     if (ahead >= 2) cp_async_wait<2>();
     else if (ahead == 1) cp_async_wait<1>();
     else cp_async_wait<0>();
