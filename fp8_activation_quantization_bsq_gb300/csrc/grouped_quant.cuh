@@ -9,7 +9,7 @@
 //  * grouped_tile_kernel (groups of many rows, prefill).  A thread block owns
 //    one 128-row scale tile, which lies inside one group, and a run of
 //    128-column tiles (k_tiles_per_block atom columns): warp 0 finds the group
-//    with a warp-parallel search over scales_offsets (rounds of 256 probes;
+//    by searching scales_offsets with all 32 lanes (rounds of 256 probes;
 //    the last round also reads row_offsets and expert_ids at the probe
 //    positions, so up to 256 groups cost one round of loads).  Then, as in
 //    the dense kernel, each lane owns one row and one 64-column half of a
@@ -31,8 +31,8 @@
 //    atom are OR-reduced over 4 lanes into one word.
 //
 // Batching column tiles per unit (k_tiles_per_block) amortizes the lookups
-// and shrinks the grid, which dominates at decode where a unit carries a few
-// routed rows.  Blocks of the last atom beyond K are zero (scale 0x00).
+// and makes the grid smaller; at decode, where each unit holds only a few
+// routed rows, the grid size is what the time depends on.  Blocks of the last atom beyond K are zero (scale 0x00).
 #pragma once
 
 #include "box_quant.cuh"

@@ -4,14 +4,14 @@
  * (tcgen05 block-scaled MMA) layout, for NVIDIA GB300 (sm_103a).
  *
  * Sources of the operations (Modular "block_scaled_quantization" pages):
- *   - module index: "block-scaled quantization kernels for NVFP4, MXFP4, and
- *     MXFP8"; block_scales_interleave "reinterleaves rank-2 scale factors into
- *     the 5D TCGEN layout"; block_scaled_matmul_with_epilogue: callers
- *     allocate the outputs;
+ *   - "block_scaled_quantization" module page, function list: quantizers
+ *     for the NVFP4, MXFP4 and MXFP8 formats; block_scales_interleave, which
+ *     rearranges rank-2 scales to the 5D TCGEN order the tensor cores read;
+ *     block_scaled_matmul_with_epilogue: callers allocate the outputs;
  *   - quantize_dynamic_scaled_async_fp4_kernel: per-group scale factors,
  *     packed FP4 elements, FP32 tensor_sf, SF_VECTOR_SIZE;
  *   - grouped_quantize_dynamic_scaled_fp4_async_kernel: per-expert tiles
- *     located by a warp-parallel search over row_offsets / scales_offsets
+ *     found by searching row_offsets / scales_offsets with a whole warp
  *     (uint32), expert_ids (int32), per-expert FP32 sf_tensor, optional int32
  *     row_indices, k_tiles_per_block column tiles per block.
  *

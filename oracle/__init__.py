@@ -8,9 +8,9 @@ does, and shares no code, table or helper with it.  Inputs come from the
 separate ``workloads`` module.
 
 Sources.  The method is the one the Modular "block_scaled_quantization" pages
-describe: "Provides block-scaled quantization kernels for NVFP4, MXFP4, and
-MXFP8" (module index), the NVFP4 kernel that "computes per-group scale
-factors and packs FP4 elements" with an FP32 ``tensor_sf`` argument
+describe: quantization of activations to the NVFP4, MXFP4 and MXFP8 block
+formats (module page), the NVFP4 kernel that derives one scale per group of
+elements and packs the FP4 codes, with an FP32 ``tensor_sf`` argument
 ("quantize_dynamic_scaled_async_fp4_kernel", description and signature), the
 grouped per-expert kernel driven by ``row_offsets``, ``scales_offsets``,
 ``expert_ids``, ``sf_tensor`` and an optional ``row_indices``

@@ -1,11 +1,11 @@
 """Block-scaled quantization steps (oracle; test infrastructure only).
 
-Follows the NVFP4 kernel's description ("computes per-group scale factors and
-packs FP4 elements", quantize_dynamic_scaled_async_fp4_kernel; FP32
-``tensor_sf`` argument and ``SF_VECTOR_SIZE`` parameter), the module's three
-formats (block_scaled_quantization module index) and the grouped kernel's
-arguments (grouped_quantize_dynamic_scaled_fp4_async_kernel signature), under
-the readings stated in the package header.
+Follows the NVFP4 kernel page (quantize_dynamic_scaled_async_fp4_kernel,
+description and signature: one scale per group of SF_VECTOR_SIZE elements,
+FP4 codes packed two per byte, an FP32 ``tensor_sf`` argument), the three
+formats named on the block_scaled_quantization module page, and the grouped
+kernel's arguments (grouped_quantize_dynamic_scaled_fp4_async_kernel,
+signature), under the readings stated in the package header.
 """
 from __future__ import annotations
 

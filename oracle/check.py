@@ -1,9 +1,10 @@
 """Consumer-side check (oracle; test infrastructure only).
 
-The module ships a "naive_block_scaled_matmul ... that emulates TCGEN
-scale-factor accumulation" (block_scaled_quantization module index): the idea
-is to check quantized operands by dequantising them through the 5D scale
-layout and taking a plain dot product.  Here that is done in float64 on the
+The block_scaled_quantization module page lists a naive reference matmul
+(naive_block_scaled_matmul) that reproduces in plain code how the tensor
+cores apply the block scales; the idea is to check quantized operands by
+dequantising them through the 5D scale layout and taking a plain dot
+product.  Here that is done in float64 on the
 CPU, reading the scales through ``scales_from_5d_view`` (a reshape statement
 of the layout, independent of the offset formula used to write them).
 """

@@ -1,8 +1,8 @@
 """5D TCGEN scale-factor layout (oracle; test infrastructure only).
 
-"block_scales_interleave: Reinterleaves rank-2 scale factors into the 5D TCGEN
-layout" (block_scaled_quantization module index) names the layout without
-giving it.  Reading: the block-scale layout the tcgen05 block-scaled MMA
+The block_scaled_quantization module page (function list,
+block_scales_interleave) names a 5D TCGEN layout that rank-2 scales are
+rearranged into, without giving it.  Reading: the block-scale layout the tcgen05 block-scaled MMA
 consumes, tiles of 128 rows x 4 scale columns (512 bytes) stored tile-row
 major, shape (Mt, Kt, 32, 4, 4) with Mt = ceil(rows/128), Kt = ceil(S/4);
 inside a tile, row r and column c sit at (r%32)*16 + (r/32)*4 + c.

@@ -1,9 +1,8 @@
 """Per-tensor and per-expert NVFP4 tensor scales (oracle; test infrastructure only).
 
 The NVFP4 kernel takes an FP32 ``tensor_sf`` (quantize_dynamic_scaled_async_fp4_kernel
-signature) and the grouped kernel a per-expert FP32 ``sf_tensor`` ("per-expert
-tensor-wise scale factor tensor", grouped_quantize_dynamic_scaled_fp4_async_kernel
-parameters).  Reading: ``tensor_sf = fl32(448 * 6 / amax)`` with amax the exact
+signature) and the grouped kernel one FP32 scale per expert in ``sf_tensor``
+(grouped_quantize_dynamic_scaled_fp4_async_kernel, argument list).  Reading: ``tensor_sf = fl32(448 * 6 / amax)`` with amax the exact
 max |x| over the tensor (over the expert's gathered rows), 1.0 for an all-zero
 tensor, so that the largest block maps onto the E4M3 maximum 448.
 """
