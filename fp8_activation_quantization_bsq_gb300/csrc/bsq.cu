@@ -26,10 +26,9 @@ constexpr int kDenseStages = 3;
 constexpr int kMaxDevices = 64;
 // Grouped quantize: groups averaging at most kGroupedLatencyMaxAvgRows rows
 // (decode) take the row kernel (kRowsPerWarp destination rows per warp),
-// larger groups (prefill) the 128-row tile kernel.
+// larger groups (prefill) the band kernel (32 destination rows per block).
 constexpr int64_t kGroupedLatencyMaxAvgRows = 16;
 constexpr int kRowsPerWarp = 2;
-constexpr int kMinTileCols = 8;  // tile kernel: at least 8 x 128 columns per block
 
 struct DeviceInfo {
   bool ready = false;
@@ -69,12 +68,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 template <int FMT>
-void grouped_tile_setup() {
-  cudaFuncSetAttribute(grouped_tile_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       kGtSmemBytes);
-}
-
-template <int FMT>
 void dense_kernel_setup(int fidx, DeviceInfo& d) {
   auto k = dense_quant_tma_kernel<FMT, kDenseStages>;
   const int smem = dense_smem_bytes<kDenseStages>();
@@ -96,9 +89,6 @@ bsq_status device_info(DeviceInfo** out) {
     dense_kernel_setup<kNVFP4>(0, d);
     dense_kernel_setup<kMXFP4>(1, d);
     dense_kernel_setup<kMXFP8>(2, d);
-    grouped_tile_setup<kNVFP4>();
-    grouped_tile_setup<kMXFP4>();
-    grouped_tile_setup<kMXFP8>();
     if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
     d.ready = true;
   }
@@ -173,21 +163,18 @@ bsq_status launch_grouped_rows(const GroupedArgs& a, cudaStream_t stream) {
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
+constexpr int kBdBlocksPerBlock = 224;  // scale blocks per band-kernel block (a multiple of 32)
+
 template <int FMT>
-bsq_status launch_grouped_tiles(GroupedArgs a, int kt, cudaStream_t stream) {
-  DeviceInfo* d = nullptr;
-  if (bsq_status st = device_info(&d); st != BSQ_OK) return st;
-  a.tiles_k = static_cast<int>(ceil_div(a.K, 128));
-  // 128-column tiles per block: k_tiles_per_block atom columns, but at least
-  // kMinTileCols so that the block's group lookup and tables are amortized
-  const int per = kt * atom_cols_of(FMT) / 128;
-  a.ktc = per > kMinTileCols ? per : kMinTileCols;
-  const int64_t chunks = ceil_div(a.tiles_k, a.ktc);
-  const int64_t tiles = a.total_scale_rows / 128;
-  if (chunks > 65535 || tiles >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
-  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(chunks));
-  const cudaError_t e =
-      launch_pdl(grouped_tile_kernel<FMT>, grid, dim3(kGtThreads), kGtSmemBytes, stream, a);
+bsq_status launch_grouped_band(GroupedArgs a, cudaStream_t stream) {
+  const int64_t s_pad = static_cast<int64_t>(a.kt_atoms) * 4;
+  a.ktc = kBdBlocksPerBlock;
+  const int64_t chunks = ceil_div(s_pad, a.ktc);
+  const int64_t blocks = ceil_div(a.total_rows, kBdRows);
+  if (chunks > 65535 || blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  if (blocks == 0) return BSQ_OK;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(chunks));
+  const cudaError_t e = launch_pdl(grouped_band_kernel<FMT>, grid, dim3(32 * band_warps<FMT>()), 0, stream, a);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -195,7 +182,7 @@ template <int FMT>
 bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t stream) {
   if (kernel == BSQ_GROUPED_AUTO)
     kernel = a.total_rows <= kGroupedLatencyMaxAvgRows * a.G ? BSQ_GROUPED_LATENCY : BSQ_GROUPED_STREAM;
-  if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_tiles<FMT>(a, kt, stream);
+  if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_band<FMT>(a, stream);
   switch (kt) {
     case 1: return launch_grouped_rows<FMT, 1>(a, stream);
     case 2: return launch_grouped_rows<FMT, 2>(a, stream);

@@ -6,21 +6,16 @@
 // scale is sf_tensor[expert_ids[g]], and it reads source row row_indices[d]
 // (or d).  Two kernels, one per regime, give identical bytes:
 //
-//  * grouped_tile_kernel (groups of many rows, prefill).  A thread block owns
-//    one 128-row scale tile, which lies inside one group, and a run of
-//    128-column tiles (k_tiles_per_block atom columns): warp 0 finds the group
-//    by searching scales_offsets with all 32 lanes (rounds of 256 probes;
-//    the last round also reads row_offsets and expert_ids at the probe
-//    positions, so up to 256 groups cost one round of loads).  Then, as in
-//    the dense kernel, each lane owns one row and one 64-column half of a
-//    tile.  Each warp streams its 32 rows' gathered segments into a 2-deep
-//    shared-memory ring with cp.async (8 lanes per row, so each instruction
-//    moves 4 rows x 128 B in whole sectors; one column tile in flight while
-//    the other is quantized, three blocks per SM; the warp waits only for its own copy groups, so
-//    the loop has no block barrier), then each lane quantizes its row from
-//    shared memory with the block's element-scale table and stores whole
-//    sectors.  Warps own 32 consecutive rows, so the unused rows of a
-//    partly filled tile are whole warps that leave at once.
+//  * grouped_band_kernel (groups of many rows, prefill).  A thread block
+//    owns 32 consecutive destination rows, whichever groups they belong to,
+//    and a run of scale blocks.  Warp 0 finds the first row's group by
+//    searching row_offsets with all 32 lanes (rounds of 256 probes), each lane
+//    steps on to its own row's group, and the distinct expert scales of the
+//    32 rows get shared element-scale tables.  Then each warp walks its rows
+//    one at a time with its 32 lanes on 32 consecutive scale blocks of the
+//    row: gathered loads and packed stores are contiguous per instruction
+//    (whole L1 lines, not one sector per lane), two steps of loads in
+//    flight, and 4 lanes OR their scale bytes into one atom word.
 //
 //  * grouped_rows_kernel (groups of a few rows, decode).  A warp owns R
 //    consecutive destination rows and one run of k_tiles_per_block atom
@@ -32,7 +27,8 @@
 //
 // Batching column tiles per unit (k_tiles_per_block) amortizes the lookups
 // and makes the grid smaller; at decode, where each unit holds only a few
-// routed rows, the grid size is what the time depends on.  Blocks of the last atom beyond K are zero (scale 0x00).
+// routed rows, the grid size is what the time depends on.  Blocks of the
+// last atom beyond K are zero (scale 0x00).
 #pragma once
 
 #include "box_quant.cuh"
@@ -60,8 +56,7 @@ struct GroupedArgs {
   int kt_atoms;         // atoms per 128-row band
   int in_vec32;         // input rows allow 32-byte loads
   int out_vec32;        // packed rows allow 32-byte stores
-  int tiles_k;          // 128-column tiles per row (tile kernel)
-  int ktc;              // 128-column tiles per thread block (tile kernel)
+  int ktc;              // scale blocks per thread block (band kernel)
 };
 
 // Checks of the offsets' first and last entries (one thread reports).
@@ -72,229 +67,211 @@ __device__ __forceinline__ void check_offsets(const GroupedArgs& a) {
     record_error(kErrValue);
 }
 
-// ------------------------------------------------------ grouped_tile_kernel --
+// ------------------------------------------------------ grouped_band_kernel --
 
-// Entry j (0..255, warp-uniform) of a 256-entry array held as 8 registers
-// per lane (entry j in register j/32 of lane j%32).
-template <typename T>
-__device__ __forceinline__ T warp_pick(const T (&reg)[8], int j) {
-  T v = reg[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i)
-    if ((j >> 5) == i) v = reg[i];
-  return __shfl_sync(0xFFFFFFFFu, v, j & 31);
-}
+// Warps per block: 8 for NVFP4, 4 for MX (the MX path holds more registers;
+// smaller blocks keep more of them resident per SM).
+template <int FMT>
+__host__ __device__ constexpr int band_warps() { return FMT == kNVFP4 ? 8 : 4; }
+constexpr int kBdMaxThreads = 256;
+constexpr int kBdRows = 32;        // destination rows per block
+constexpr int kBdTables = 2;       // distinct tensor scales of the band with a shared element-scale table
 
-struct TileInfo {
-  int64_t dst0;   // destination row of the tile's first row
-  int n;          // rows of the tile to quantize (0: none)
-  int e;          // expert id
+struct BdRow {
+  int64_t src;       // source row
+  int64_t dst;       // destination row
+  int64_t band;      // byte offset of the row's 128-row band in the 5D scales
+  int atom_off;      // the row's word inside an atom
+  int tab;           // factor table slot, -1: divide
+  float tsf;
+  int ok;            // quantize this row
 };
 
-// Resolve the 128-row scale tile starting at row0 (warp-collective):
-// g = max{g : so[g] <= row0}, then the tile's rows in group g.  Inconsistent
-// metadata records BSQ_ERR_VALUE and leaves the tile empty.
-__device__ __forceinline__ TileInfo resolve_tile(const GroupedArgs& a, int64_t row0) {
-  const uint32_t* so = a.scales_offsets;
+// g = max{g : row_offsets[g] <= d} for a warp-uniform d: rounds of 256
+// probes (8 per lane) narrow [lo, hi) until it holds one group.
+__device__ __forceinline__ int band_group_of(const GroupedArgs& a, int64_t d) {
   const int lane = threadIdx.x & 31;
-  int lo = 0, hi = a.G;
-  while (hi - lo > 256) {
+  int lo = 0, hi = a.G;  // ro[lo] <= d < ro[hi] (ro[G] > d is guaranteed by the caller)
+  while (hi - lo > 1) {
     const int step = (hi - lo + 255) >> 8;
     int cnt = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t pos = lo + static_cast<int64_t>(step) * (1 + lane + 32 * i);
-      cnt += __popc(__ballot_sync(0xFFFFFFFFu, pos < hi && static_cast<int64_t>(__ldg(so + pos)) <= row0));
+      cnt += __popc(__ballot_sync(0xFFFFFFFFu, pos < hi && static_cast<int64_t>(__ldg(a.row_offsets + pos)) <= d));
     }
     const int nlo = lo + cnt * step;
     hi = min(hi, nlo + step);
     lo = nlo;
   }
-  // final round: positions lo+1 .. lo+256 (so / ro up to G, expert ids below G)
-  uint32_t so_p[8], ro_p[8];
-  int32_t e_p[8];
-  int cnt = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int pos = lo + 1 + lane + 32 * i;
-    so_p[i] = pos <= a.G ? __ldg(so + pos) : 0xFFFFFFFFu;
-    ro_p[i] = pos <= a.G ? __ldg(a.row_offsets + pos) : 0u;
-    e_p[i] = pos < a.G ? __ldg(a.expert_ids + pos) : -1;
-  }
-  const int64_t so0 = __ldg(so), so_end = __ldg(so + a.G);
-  const uint32_t so_lo = __ldg(so + lo), ro_lo = __ldg(a.row_offsets + lo);
-  const int32_t e_lo = __ldg(a.expert_ids + lo);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    cnt += __popc(__ballot_sync(0xFFFFFFFFu, lo + 1 + lane + 32 * i < hi &&
-                                                 static_cast<int64_t>(so_p[i]) <= row0));
-  // g = lo + cnt: entry g sits at probe index cnt-1, entry g+1 at index cnt
-  const int64_t so_g = cnt == 0 ? so_lo : warp_pick(so_p, cnt - 1);
-  const int64_t r_beg = cnt == 0 ? ro_lo : warp_pick(ro_p, cnt - 1);
-  const int e = cnt == 0 ? e_lo : warp_pick(e_p, cnt - 1);
-  const int64_t so_n = warp_pick(so_p, cnt);
-  const int64_t r_end = warp_pick(ro_p, cnt);
-
-  TileInfo t{0, 0, -1};
-  if (so0 != 0 || row0 >= so_end) return t;
-  const int64_t m_g = r_end - r_beg;
-  const int64_t i0 = row0 - so_g;
-  if (m_g < 0 || m_g > so_n - so_g || r_end > a.total_rows) {
-    if (lane == 0) record_error(kErrValue);
-    return t;
-  }
-  if (i0 >= m_g || e < 0) return t;  // padding tile, or a skipped group
-  if (a.sf != nullptr && e >= a.num_experts) {
-    if (lane == 0) record_error(kErrValue);
-    return t;
-  }
-  t.dst0 = r_beg + i0;
-  t.n = static_cast<int>(m_g - i0 < 128 ? m_g - i0 : 128);
-  t.e = e;
-  return t;
+  return lo;
 }
 
-constexpr int kGtWarps = 8;
-constexpr int kGtThreads = 32 * kGtWarps;
-constexpr int kGtPitch = 272;                     // bytes per staged row: 2 x 128 + 16 pad
-constexpr int kGtStageBytes = 128 * kGtPitch;
-// Two stages (one column tile in flight while one is quantized) and three
-// resident blocks per SM: 24 warps per SM hide the gather and arithmetic
-// latency better than three stages at two blocks per SM (shared memory
-// limits residency to 2 blocks at 3 stages).
-constexpr int kGtStages = 2;                      // 1 to 3
-constexpr int kGtMinBlocks = 3;                   // resident blocks per SM (launch bounds)
-constexpr int kGtSmemBytes = kGtStages * kGtStageBytes;
-
-struct GtShared {
-  TileInfo tile;
-  float factor_tab[256];
-  float div6_tab[128];
-  int64_t src[128];  // source row of each tile row, -1 when invalid
-};
-
-// 16-byte asynchronous global -> shared copy, cached in L2 only.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// A warp's gathered copies of one 64-column half of a column tile: in copy k
-// (0..7) lane l moves 16-byte chunk cc = l % 8 of tile row crow0 + 4k (crow0 =
-// the warp's first row + l / 8) from source row csrc[k] (skipped when < 0).
-// One commit group per call, empty beyond K, keeps wait_group counts exact.
-__device__ __forceinline__ void gt_issue(const GroupedArgs& a, uint8_t* stage_half, int col0, int cc,
-                                         int crow0, const int64_t (&csrc)[8]) {
-  if (col0 < a.K && cc < (a.K - col0) / 8) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (csrc[k] >= 0)
-        cp_async16(stage_half + (crow0 + 4 * k) * kGtPitch + 16 * cc, a.in + csrc[k] * a.ld_in + col0 + 8 * cc);
-  }
-  cp_async_commit();
-}
-
+// Quantize one scale block held in registers (SF elements) to dst; returns
+// the block's scale byte.
 template <int FMT>
-__global__ void __launch_bounds__(kGtThreads, kGtMinBlocks) grouped_tile_kernel(const GroupedArgs a) {
-  __shared__ GtShared sh;
-  extern __shared__ __align__(128) uint8_t ring[];
+__device__ __forceinline__ uint32_t band_block(const uint4 (&v)[Fmt<FMT>::SF / 8], uint8_t* dst, bool out_vec32,
+                                               const NvScale& ns) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < Fmt<FMT>::SF / 8; ++c) {
+    acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
+    acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
+  }
+  const float amax = absmax_final(acc);
+  if constexpr (FMT == kNVFP4) {
+    const BlockScale sc = nvfp4_block_scale(amax, ns);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(quant8_e2m1(v[0], sc.factor), quant8_e2m1(v[1], sc.factor));
+    return sc.byte;
+  } else if constexpr (FMT == kMXFP4) {
+    const MxScale sc = mx_scale<6>(amax);
+    st_global_v4(dst, quant8_e2m1_pow2(v[0], sc.pow2), quant8_e2m1_pow2(v[1], sc.pow2),
+                 quant8_e2m1_pow2(v[2], sc.pow2), quant8_e2m1_pow2(v[3], sc.pow2));
+    return sc.byte;
+  } else {
+    const MxScale sc = mx_scale<448>(amax);
+    uint32_t o[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint2 q = quant8_e4m3_pow2(v[c], sc.pow2);
+      o[2 * c] = q.x;
+      o[2 * c + 1] = q.y;
+    }
+    if (out_vec32) {
+      st_global_v8(dst, o);
+    } else {
+      st_global_v4(dst, o[0], o[1], o[2], o[3]);
+      st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
+    }
+    return sc.byte;
+  }
+}
+
+// One scale block of a row from global memory (SF BF16 elements).
+template <int SF>
+__device__ __forceinline__ void band_load(uint4 (&v)[SF / 8], const uint16_t* p, bool vec32) {
+  if (vec32) {
+#pragma unroll
+    for (int c = 0; c < SF / 8; c += 2) ld_global_nc_v8(p + 8 * c, v[c], v[c + 1]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < SF / 8; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
+  }
+}
+
+// A block owns kBdRows consecutive destination rows (across group boundaries)
+// and a run of a.ktc scale blocks (a multiple of 32).  Warp 0 resolves the
+// rows: one warp-wide search for the first row's group, then each lane steps
+// forward to its own row's group; the first kBdTables distinct tensor scales
+// among the rows get a 256-entry element-scale table (NVFP4).  Warp w then
+// takes rows w, w + kBdWarps, ...: for each, the 32 lanes hold 32 consecutive
+// scale blocks of the row (coalesced loads and stores, the blocks two steps
+// ahead in flight), and 4 lanes OR their scale bytes into one atom word.
+template <int FMT>
+__global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(const GroupedArgs a) {
+  constexpr int SF = Fmt<FMT>::SF;
+  constexpr int kBdWarps = band_warps<FMT>();
+  constexpr int kBdThreads = 32 * kBdWarps;
+  __shared__ BdRow rows[kBdRows];
+  __shared__ float factor_tab[kBdTables][256];
+  __shared__ float div6_tab[128];
+  __shared__ float tab_tsf[kBdTables];
+  __shared__ int n_tabs;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
+  const int64_t d0 = static_cast<int64_t>(blockIdx.x) * kBdRows;
+  if constexpr (FMT == kNVFP4) fill_div6_table(div6_tab, threadIdx.x, kBdThreads);
   pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_offsets(a);
 
+  // ---- rows of the band (warp 0)
   if (warp == 0) {
-    const TileInfo t = resolve_tile(a, static_cast<int64_t>(tile) * 128);
-    if (lane == 0) {
-      sh.tile = t;
-      if (tile == 0 && blockIdx.y == 0) check_offsets(a);
-    }
-  } else if (FMT == kNVFP4) {
-    fill_div6_table(sh.div6_tab, threadIdx.x - 32, kGtThreads - 32);
-  }
-  __syncthreads();
-  const TileInfo t = sh.tile;
-  if (t.n == 0) return;
-
-  // tile rows' sources (and the NVFP4 element-scale table of the expert)
-  if (threadIdx.x < 128) {
-    int64_t src = -1;
-    if (static_cast<int>(threadIdx.x) < t.n) {
-      const int64_t d = t.dst0 + threadIdx.x;
-      src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
-      if (src < 0 || src >= a.in_rows) {
-        record_error(kErrValue);
-        src = -1;
-      }
-    }
-    sh.src[threadIdx.x] = src;
-  }
-  float tsf = 1.0f;
-  if constexpr (FMT == kNVFP4) {
-    tsf = __ldg(a.sf + t.e);
-    fill_nvfp4_factor_table(sh.factor_tab, tsf, threadIdx.x, kGtThreads);
-  }
-  __syncthreads();
-
-  // warp -> (64-column half h, rows 32*(warp%4) ...+31); lane -> one row
-  const int h = warp >> 2;
-  const int wr = 32 * (warp & 3);                  // first tile row of this warp
-  if (wr >= t.n) return;                           // no block barrier follows
-  const int row = wr + lane;
-  const bool row_ok = row < t.n && sh.src[row] >= 0;
-  const NvScale ns{tsf, sh.factor_tab, nullptr, sh.div6_tab};
-  uint8_t* out_row = a.out + (t.dst0 + row) * a.out_ld;
-  uint8_t* band = a.scales + static_cast<int64_t>(tile) * a.kt_atoms * 512 + lane * 16 + (warp & 3) * 4;
-
-  // copy role: in copy k (0..7) lane l moves chunk l%8 of row wr + l/8 + 4k
-  const int cc = lane & 7;
-  int64_t csrc[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int crow = wr + (lane >> 3) + 4 * k;
-    csrc[k] = crow < t.n ? sh.src[crow] : -1;
-  }
-
-  const int kt_beg = blockIdx.y * a.ktc;
-  const int kt_end = min(a.tiles_k, kt_beg + a.ktc);
-  auto issue = [&](int kt) {
-    gt_issue(a, ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + h * 128, kt * 128 + 64 * h, cc,
-             wr + (lane >> 3), csrc);
-  };
-  constexpr int kAhead = kGtStages - 1;        // column tiles in flight while one is quantized
-#pragma unroll
-  for (int i = 0; i < kAhead; ++i)
-    if (kt_beg + i < kt_end) issue(kt_beg + i);
-#pragma unroll 1
-  for (int kt = kt_beg; kt < kt_end; ++kt) {
-    const int ahead = min(kAhead, kt_end - 1 - kt);  // groups committed after tile kt
-    if (kt + kAhead < kt_end) issue(kt + kAhead);     // into the slot freed kAhead tiles ago
-    if (ahead >= 2) cp_async_wait<2>();
-    else if (ahead == 1) cp_async_wait<1>();
-    else cp_async_wait<0>();
-    __syncwarp();                               // the warp's copies are visible to all its lanes
-    const int col0 = kt * 128 + 64 * h;
-    if (col0 < a.K) {
-      if (row_ok) {
-        uint8_t* dst = out_row + (Fmt<FMT>::OUT_BITS == 4 ? (col0 >> 1) : col0);
-        const uint32_t sbytes = quant_box_row<FMT, false>(
-            ring + ((kt - kt_beg) % kGtStages) * kGtStageBytes + row * kGtPitch + h * 128, row,
-            min(64, a.K - col0), dst, a.out_vec32 != 0, ns);
-        if constexpr (FMT == kNVFP4) {
-          *reinterpret_cast<uint32_t*>(band + (2 * kt + h) * 512) = sbytes;
-        } else {
-          *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = static_cast<uint16_t>(sbytes);
+    const int64_t d = d0 + lane;
+    BdRow st{0, d, 0, 0, -1, 1.0f, 0};
+    const int64_t ro_end = static_cast<int64_t>(__ldg(a.row_offsets + a.G));
+    const int64_t d_lim = ro_end < a.total_rows ? ro_end : a.total_rows;  // rows inside groups
+    if (d0 < d_lim) {
+      int g = band_group_of(a, d0);
+      if (d < d_lim) {
+        // step forward to this row's group (consecutive rows: a few groups at most)
+        while (g + 1 < a.G && static_cast<int64_t>(__ldg(a.row_offsets + g + 1)) <= d) ++g;
+        const int64_t r_beg = __ldg(a.row_offsets + g), r_end = __ldg(a.row_offsets + g + 1);
+        const int64_t so_g = __ldg(a.scales_offsets + g), so_n = __ldg(a.scales_offsets + g + 1);
+        const int e = __ldg(a.expert_ids + g);
+        const int64_t srow = so_g + (d - r_beg);
+        if (r_end - r_beg < 0 || r_end - r_beg > so_n - so_g || r_end > a.total_rows ||
+            srow >= a.total_scale_rows || d < r_beg || d >= r_end ||
+            (a.sf != nullptr && e >= a.num_experts)) {
+          record_error(kErrValue);
+        } else if (e >= 0) {
+          const int64_t src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
+          if (src < 0 || src >= a.in_rows) {
+            record_error(kErrValue);
+          } else {
+            st.src = src;
+            st.band = (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512;
+            st.atom_off = static_cast<int>((srow & 31) * 16 + ((srow & 127) >> 5) * 4);
+            st.ok = 1;
+            if (a.sf != nullptr) st.tsf = __ldg(a.sf + e);
+          }
         }
       }
-    } else if constexpr (FMT != kNVFP4) {
-      if (row_ok) *reinterpret_cast<uint16_t*>(band + kt * 512 + 2 * h) = 0;  // blocks beyond K
     }
-    __syncwarp();                               // slot reads done before it is refilled
+    if constexpr (FMT == kNVFP4) {
+      // table slots: the lowest lane of each distinct tensor scale leads its
+      // lanes; leaders in lane order take the first kBdTables slots
+      const uint32_t key = st.ok ? __float_as_uint(st.tsf) : 0xFFFFFFFFu;
+      const uint32_t same = __match_any_sync(0xFFFFFFFFu, key);
+      const int leader = __ffs(same) - 1;
+      const uint32_t leaders = __ballot_sync(0xFFFFFFFFu, st.ok && leader == lane);
+      const int rank = __popc(leaders & ((1u << leader) - 1u));
+      st.tab = st.ok && rank < kBdTables ? rank : -1;
+      if (st.ok && leader == lane && rank < kBdTables) tab_tsf[rank] = st.tsf;
+      if (lane == 0) n_tabs = min(__popc(leaders), kBdTables);
+    }
+    rows[lane] = st;
+  }
+  __syncthreads();
+  if constexpr (FMT == kNVFP4) {
+    for (int t = 0; t < n_tabs; ++t) fill_nvfp4_factor_table(factor_tab[t], tab_tsf[t], threadIdx.x, kBdThreads);
+    __syncthreads();
+  }
+
+  // ---- quantize: warp -> rows, lane -> scale blocks
+  const int S = a.K / SF;                       // scale blocks per row
+  const int s_pad = a.kt_atoms * 4;             // blocks per row with the last atom's padding
+  const int blk_beg = blockIdx.y * a.ktc;
+  const int blk_end = min(s_pad, blk_beg + a.ktc);
+  const bool in_vec32 = a.in_vec32 != 0, out_vec32 = a.out_vec32 != 0;
+  for (int r = warp; r < kBdRows; r += kBdWarps) {
+    const BdRow row = rows[r];
+    if (!row.ok) continue;  // warp-uniform
+    const uint16_t* in_row = a.in + row.src * a.ld_in;
+    uint8_t* out_row = a.out + row.dst * a.out_ld;
+    uint8_t* scale_row = a.scales + row.band + row.atom_off;
+    const NvScale ns{row.tsf, row.tab >= 0 ? factor_tab[row.tab] : nullptr, nullptr, div6_tab};
+    // blocks blk0 + lane for blk0 = blk_beg, blk_beg + 32, ...; two steps in flight
+    uint4 v0[SF / 8], v1[SF / 8];
+    if (blk_beg + lane < S) band_load<SF>(v0, in_row + static_cast<int64_t>(blk_beg + lane) * SF, in_vec32);
+    if (blk_beg + 32 + lane < min(S, blk_end)) band_load<SF>(v1, in_row + static_cast<int64_t>(blk_beg + 32 + lane) * SF, in_vec32);
+#pragma unroll 1
+    for (int blk0 = blk_beg; blk0 < blk_end; blk0 += 32) {
+      const int blk = blk0 + lane;
+      uint4 v[SF / 8];
+#pragma unroll
+      for (int c = 0; c < SF / 8; ++c) { v[c] = v0[c]; v0[c] = v1[c]; }
+      const int nb = blk + 64;
+      if (nb < S && blk0 + 64 < blk_end) band_load<SF>(v1, in_row + static_cast<int64_t>(nb) * SF, in_vec32);
+      uint32_t sbyte = 0;
+      if (blk < S && blk < blk_end)
+        sbyte = band_block<FMT>(v, out_row + (Fmt<FMT>::OUT_BITS == 4 ? (blk * SF) >> 1 : blk * SF), out_vec32, ns);
+      // scale word of atom blk/4: byte blk%4 from lanes 4j..4j+3
+      uint32_t word = sbyte << (8 * (lane & 3));
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+      if ((lane & 3) == 0 && blk < blk_end)
+        *reinterpret_cast<uint32_t*>(scale_row + static_cast<int64_t>(blk >> 2) * 512) = word;
+    }
   }
 }
 

@@ -165,7 +165,8 @@ BSQ_API int32_t bsq_grouped_quantize(int32_t fmt, const void* in_dev, int64_t in
 /* Kernel of the grouped quantize. */
 typedef enum {
   BSQ_GROUPED_AUTO = 0,    /* LATENCY when total_rows <= 16 * G, else STREAM */
-  BSQ_GROUPED_STREAM = 1,  /* one thread block per 128-row scale tile (groups of many rows) */
+  BSQ_GROUPED_STREAM = 1,  /* one thread block per 32 destination rows x a run of scale blocks,
+                              a warp per row at a time (groups of many rows) */
   BSQ_GROUPED_LATENCY = 2  /* one warp per 2 destination rows (groups of a few rows) */
 } bsq_grouped_kernel;
 
