@@ -305,12 +305,13 @@ def extra_workloads(bsq, device, flush, peak):
     res["grouped_tensor_sf_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2),
                                                     "gathered_GB_s": round(d["total_rows"] * d["K"] * 2 / (mean * 1e6), 1)}
     del xg, gsf, gws
-    for kt in (8,):
-        mean, mn, b = grouped(d, "nvfp4", kt, "prefill", uniq)
-        res[f"nvfp4_grouped_prefill_T4096_K7168_kt{kt}"] = {
+    for fmt in ("nvfp4", "mxfp8", "mxfp4"):
+        mean, mn, b = grouped(d, fmt, 8, "prefill", uniq)
+        res[f"{fmt}_grouped_prefill_T4096_K7168"] = {
             "GB_s": round(b / (mean * 1e6), 1), "us": round(mean * 1e3, 2),
             "frac_of_hbm": round(b / (mean * 1e6) / peak, 3), "algorithmic_bytes": b,
-            "logical_input_bytes": d["total_rows"] * d["K"] * 2}
+            "logical_input_bytes": d["total_rows"] * d["K"] * 2,
+            "T_elements_per_s": round(d["total_rows"] * d["K"] / (mean * 1e-3) / 1e12, 2)}
     del d
     for fmt in ("nvfp4", "mxfp8"):
         for K in (7168, 2048):

@@ -236,3 +236,33 @@ def test_grouped_source_rows_with_many_copies(bsq, fmt, K, kernel):
     d = dict(d, row_indices=ridx)
     p, s = _run_grouped(bsq, fmt, d, 1, kernel=kernel)
     _compare(fmt, d, p, s)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_strided_input_and_16_byte_aligned_outputs(bsq, fmt, kernel):
+    """The 16-byte load and store paths: input rows with a stride of K + 8
+    elements (not a multiple of 32 bytes) and packed / scale outputs that
+    start 16 bytes past a 32-byte boundary."""
+    d = wl.config_grouped_prefill(seed=10, tokens=90, K=288, num_experts=12, top_k=3)
+    K = d["K"]
+    wide = np.zeros((d["x_bits"].shape[0], K + 8), np.uint16)
+    wide[:, :K] = d["x_bits"]
+    wide[:, K:] = 0x7F00                          # huge values outside the view
+    x = to_device_bf16(wide)[:, :K]
+    total_rows, tsr = d["total_rows"], d["total_scale_rows"]
+    ob = total_rows * oracle.packed_row_bytes(fmt, K)
+    sb = oracle.scales5d_bytes(tsr, K // oracle.block_size(fmt))
+    ofull, _ = guarded(ob + 16)
+    sfull, _ = guarded(sb + 16)
+    out, sc = ofull[16:16 + ob], sfull[16:16 + sb]
+    assert out.data_ptr() % 32 == 16 and sc.data_ptr() % 32 == 16
+    bsq.grouped_quantize(x, fmt, u32_device(d["row_offsets"]), u32_device(d["scales_offsets"]),
+                         i32_device(d["expert_ids"]),
+                         torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
+                         i32_device(d["row_indices"]), total_rows=total_rows, total_scale_rows=tsr,
+                         k_tiles_per_block=2, out=out, scales=sc, kernel=kernel)
+    assert bsq.device_error() == 0
+    assert margin_intact(ofull) and margin_intact(sfull)
+    assert np.all(ofull[:16].cpu().numpy() == SENTINEL) and np.all(sfull[:16].cpu().numpy() == SENTINEL)
+    _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy())
