@@ -339,6 +339,24 @@ __device__ __forceinline__ void ld_global_nc_v8(const void* p, uint4& lo, uint4&
                : "l"(p));
 }
 
+// L2 cache policy for loads: keep the lines (evict_last) for a following
+// pass over the same data -- the tensor-scale reduction before quantizing
+// the same tensor.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Read-only 16-byte global load, no L1 allocation, with an L2 policy.
+__device__ __forceinline__ uint4 ld_global_nc_v4_policy(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
 // Read-only 16-byte global load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 r;

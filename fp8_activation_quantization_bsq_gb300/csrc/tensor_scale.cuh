@@ -37,20 +37,22 @@ __device__ __forceinline__ float tensor_sf_of(float amax) {
 }
 
 // max |x| over one row of K BF16 elements (K % 8 == 0), as two BF16 halves.
-__device__ __forceinline__ uint32_t row_absmax(const uint16_t* row, int K, int lane) {
+// The loads keep their lines in L2 (evict_last) for the quantize pass that
+// follows over the same tensor.
+__device__ __forceinline__ uint32_t row_absmax(const uint16_t* row, int K, int lane, uint64_t pol) {
   uint32_t acc = 0;
   const int chunks = K >> 3;
   int c = lane;
   for (; c + 96 < chunks; c += 128) {
-    const uint4 v0 = ld_global_nc_v4(row + 8 * c), v1 = ld_global_nc_v4(row + 8 * (c + 32));
-    const uint4 v2 = ld_global_nc_v4(row + 8 * (c + 64)), v3 = ld_global_nc_v4(row + 8 * (c + 96));
+    const uint4 v0 = ld_global_nc_v4_policy(row + 8 * c, pol), v1 = ld_global_nc_v4_policy(row + 8 * (c + 32), pol);
+    const uint4 v2 = ld_global_nc_v4_policy(row + 8 * (c + 64), pol), v3 = ld_global_nc_v4_policy(row + 8 * (c + 96), pol);
     acc = absmax2(acc, v0.x); acc = absmax2(acc, v0.y); acc = absmax2(acc, v0.z); acc = absmax2(acc, v0.w);
     acc = absmax2(acc, v1.x); acc = absmax2(acc, v1.y); acc = absmax2(acc, v1.z); acc = absmax2(acc, v1.w);
     acc = absmax2(acc, v2.x); acc = absmax2(acc, v2.y); acc = absmax2(acc, v2.z); acc = absmax2(acc, v2.w);
     acc = absmax2(acc, v3.x); acc = absmax2(acc, v3.y); acc = absmax2(acc, v3.z); acc = absmax2(acc, v3.w);
   }
   for (; c < chunks; c += 32) {
-    const uint4 v = ld_global_nc_v4(row + 8 * c);
+    const uint4 v = ld_global_nc_v4_policy(row + 8 * c, pol);
     acc = absmax2(acc, v.x); acc = absmax2(acc, v.y); acc = absmax2(acc, v.z); acc = absmax2(acc, v.w);
   }
   return acc;
@@ -71,9 +73,10 @@ __global__ void __launch_bounds__(kAmaxThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   uint32_t acc = 0;
+  const uint64_t pol = l2_policy_evict_last();
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kAmaxWarps + warp; r < M;
        r += static_cast<int64_t>(gridDim.x) * kAmaxWarps)
-    acc = absmax2(acc, row_absmax(in + r * ld, K, lane));
+    acc = absmax2(acc, row_absmax(in + r * ld, K, lane, pol));
   const uint32_t wm = warp_max_bits(__float_as_uint(absmax_final(acc)));
   if (lane == 0) warp_max[warp] = wm;
   __syncthreads();
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
   pdl_wait();
   const int64_t ro_end = a.G > 0 ? static_cast<int64_t>(__ldg(a.row_offsets + a.G)) : 0;  // no groups: no rows
   const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  const uint64_t pol = l2_policy_evict_last();
   for (int64_t d = static_cast<int64_t>(blockIdx.x) * kAmaxWarps + warp; d < rows;
        d += static_cast<int64_t>(gridDim.x) * kAmaxWarps) {
     int e = -1;
@@ -149,7 +153,8 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
     e = __shfl_sync(0xFFFFFFFFu, e, 0);
     src = __shfl_sync(0xFFFFFFFFu, src, 0);
     if (e < 0) continue;  // warp-uniform
-    const uint32_t m = warp_max_bits(__float_as_uint(absmax_final(row_absmax(a.in + src * a.ld_in, a.K, lane))));
+    const uint32_t m =
+        warp_max_bits(__float_as_uint(absmax_final(row_absmax(a.in + src * a.ld_in, a.K, lane, pol))));
     if (lane == 0 && m != 0u) atomicMax(a.amax_bits + e, m);
   }
   __syncthreads();
