@@ -163,13 +163,13 @@ bsq_status launch_grouped_rows(const GroupedArgs& a, cudaStream_t stream) {
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
-constexpr int kBdBlocksPerBlock = 224;  // scale blocks per band-kernel block (a multiple of 32)
+constexpr int kBdChunksPerBlock = 224;  // 32-element chunks per band-kernel block (a multiple of 32)
 
 template <int FMT>
 bsq_status launch_grouped_band(GroupedArgs a, cudaStream_t stream) {
-  const int64_t s_pad = static_cast<int64_t>(a.kt_atoms) * 4;
-  a.ktc = kBdBlocksPerBlock;
-  const int64_t chunks = ceil_div(s_pad, a.ktc);
+  const int64_t c_pad = static_cast<int64_t>(a.kt_atoms) * (FMT == kNVFP4 ? 2 : 4);
+  a.ktc = kBdChunksPerBlock;
+  const int64_t chunks = ceil_div(c_pad, a.ktc);
   const int64_t blocks = ceil_div(a.total_rows, kBdRows);
   if (chunks > 65535 || blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   if (blocks == 0) return BSQ_OK;

@@ -56,7 +56,7 @@ struct GroupedArgs {
   int kt_atoms;         // atoms per 128-row band
   int in_vec32;         // input rows allow 32-byte loads
   int out_vec32;        // packed rows allow 32-byte stores
-  int ktc;              // scale blocks per thread block (band kernel)
+  int ktc;              // 32-element chunks per thread block (band kernel)
 };
 
 // Checks of the offsets' first and last entries (one thread reports).
@@ -69,10 +69,10 @@ __device__ __forceinline__ void check_offsets(const GroupedArgs& a) {
 
 // ------------------------------------------------------ grouped_band_kernel --
 
-// Warps per block: 8 for NVFP4, 4 for MX (the MX path holds more registers;
-// smaller blocks keep more of them resident per SM).
+// Warps per block: 4 (with 63-70 registers per thread, blocks of 4 warps
+// keep 6-7 blocks resident per SM).
 template <int FMT>
-__host__ __device__ constexpr int band_warps() { return FMT == kNVFP4 ? 8 : 4; }
+__host__ __device__ constexpr int band_warps() { return 4; }
 constexpr int kBdMaxThreads = 256;
 constexpr int kBdRows = 32;        // destination rows per block
 constexpr int kBdTables = 2;       // distinct tensor scales of the band with a shared element-scale table
@@ -107,10 +107,10 @@ __device__ __forceinline__ int band_group_of(const GroupedArgs& a, int64_t d) {
   return lo;
 }
 
-// Quantize one scale block held in registers (SF elements) to dst; returns
-// the block's scale byte.
+// Quantize one MX scale block held in registers (32 elements) to dst;
+// returns the block's scale byte.
 template <int FMT>
-__device__ __forceinline__ uint32_t band_block(const uint4 (&v)[Fmt<FMT>::SF / 8], uint8_t* dst, bool out_vec32,
+__device__ __forceinline__ uint32_t band_block(const uint4 (&v)[4], uint8_t* dst, bool out_vec32,
                                                const NvScale& ns) {
   uint32_t acc = 0;
 #pragma unroll
@@ -147,26 +147,71 @@ __device__ __forceinline__ uint32_t band_block(const uint4 (&v)[Fmt<FMT>::SF / 8
   }
 }
 
-// One scale block of a row from global memory (SF BF16 elements).
-template <int SF>
-__device__ __forceinline__ void band_load(uint4 (&v)[SF / 8], const uint16_t* p, bool vec32) {
+// One 32-element chunk of a row from global memory (64 bytes).
+__device__ __forceinline__ void band_load(uint4 (&v)[4], const uint16_t* p, bool vec32) {
   if (vec32) {
-#pragma unroll
-    for (int c = 0; c < SF / 8; c += 2) ld_global_nc_v8(p + 8 * c, v[c], v[c + 1]);
+    ld_global_nc_v8(p, v[0], v[1]);
+    ld_global_nc_v8(p + 16, v[2], v[3]);
   } else {
 #pragma unroll
-    for (int c = 0; c < SF / 8; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
+    for (int c = 0; c < 4; ++c) v[c] = ld_global_nc_v4(p + 8 * c);
   }
 }
 
+// Quantize one 32-element chunk of a row held in registers (two NVFP4
+// blocks or one MX block) to dst; returns its scale bytes (NVFP4: block 0 in
+// bits 0-7, block 1 in bits 8-15).
+template <int FMT>
+__device__ __forceinline__ uint32_t band_chunk(const uint4 (&v)[4], uint8_t* dst, bool out_vec32, const NvScale& ns) {
+  if constexpr (FMT == kNVFP4) {
+    uint32_t o[4], bytes = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int c = 2 * j; c < 2 * j + 2; ++c) {
+        acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
+        acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
+      }
+      const BlockScale sc = nvfp4_block_scale(absmax_final(acc), ns);
+      o[2 * j] = quant8_e2m1(v[2 * j], sc.factor);
+      o[2 * j + 1] = quant8_e2m1(v[2 * j + 1], sc.factor);
+      bytes |= sc.byte << (8 * j);
+    }
+    st_global_v4(dst, o[0], o[1], o[2], o[3]);
+    return bytes;
+  } else {
+    return band_block<FMT>(v, dst, out_vec32, ns);
+  }
+}
+
+// One chunk step of a band row: lane chunk ch (< c_end), data in v; the
+// lanes of one atom OR their scale bytes into its word.
+template <int FMT>
+__device__ __forceinline__ void band_chunk_step(const uint4 (&v)[4], int ch, int n_chunks, int c_end,
+                                                uint8_t* out_row, uint8_t* scale_row, bool out_vec32,
+                                                const NvScale& ns) {
+  constexpr int BPL = 32 / Fmt<FMT>::SF;  // scale blocks per chunk
+  constexpr int CPA = 4 / BPL;            // chunks per atom
+  const int lane = threadIdx.x & 31;
+  uint32_t bytes = 0;  // padding blocks of the last atom stay 0x00
+  if (ch < n_chunks && ch < c_end)
+    bytes = band_chunk<FMT>(v, out_row + (Fmt<FMT>::OUT_BITS == 4 ? 16 * ch : 32 * ch), out_vec32, ns);
+  uint32_t word = bytes << (8 * BPL * (lane % CPA));
+#pragma unroll
+  for (int m = 1; m < CPA; m <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, m);
+  if (lane % CPA == 0 && ch < c_end) *reinterpret_cast<uint32_t*>(scale_row + (ch / CPA) * 512) = word;
+}
+
 // A block owns kBdRows consecutive destination rows (across group boundaries)
-// and a run of a.ktc scale blocks (a multiple of 32).  Warp 0 resolves the
+// and a run of a.ktc 32-element chunks (a multiple of 32).  Warp 0 resolves the
 // rows: one warp-wide search for the first row's group, then each lane steps
 // forward to its own row's group; the first kBdTables distinct tensor scales
 // among the rows get a 256-entry element-scale table (NVFP4).  Warp w then
 // takes rows w, w + kBdWarps, ...: for each, the 32 lanes hold 32 consecutive
-// scale blocks of the row (coalesced loads and stores, the blocks two steps
-// ahead in flight), and 4 lanes OR their scale bytes into one atom word.
+// 32-element chunks of the row (two NVFP4 or one MX scale block each: 2 KB
+// of contiguous loads and 512 B / 1 KB of contiguous stores per step), and
+// the lanes of one atom OR their scale bytes into its word.
 template <int FMT>
 __global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(const GroupedArgs a) {
   constexpr int SF = Fmt<FMT>::SF;
@@ -237,11 +282,13 @@ __global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(co
     __syncthreads();
   }
 
-  // ---- quantize: warp -> rows, lane -> scale blocks
-  const int S = a.K / SF;                       // scale blocks per row
-  const int s_pad = a.kt_atoms * 4;             // blocks per row with the last atom's padding
-  const int blk_beg = blockIdx.y * a.ktc;
-  const int blk_end = min(s_pad, blk_beg + a.ktc);
+  // ---- quantize: warp -> rows, lane -> 32-element chunks
+  constexpr int CPA = 4 / (32 / SF);            // chunks per 5D atom
+  const int n_chunks = a.K / 32;                // chunks per row
+  const int c_pad = a.kt_atoms * CPA;           // with the last atom's padding
+  const int c_beg = blockIdx.y * a.ktc;
+  const int c_end = min(c_pad, c_beg + a.ktc);
+  const int lim = min(n_chunks, c_end);         // chunks with data
   const bool in_vec32 = a.in_vec32 != 0, out_vec32 = a.out_vec32 != 0;
   for (int r = warp; r < kBdRows; r += kBdWarps) {
     const BdRow row = rows[r];
@@ -250,27 +297,33 @@ __global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(co
     uint8_t* out_row = a.out + row.dst * a.out_ld;
     uint8_t* scale_row = a.scales + row.band + row.atom_off;
     const NvScale ns{row.tsf, row.tab >= 0 ? factor_tab[row.tab] : nullptr, nullptr, div6_tab};
-    // blocks blk0 + lane for blk0 = blk_beg, blk_beg + 32, ...; two steps in flight
-    uint4 v0[SF / 8], v1[SF / 8];
-    if (blk_beg + lane < S) band_load<SF>(v0, in_row + static_cast<int64_t>(blk_beg + lane) * SF, in_vec32);
-    if (blk_beg + 32 + lane < min(S, blk_end)) band_load<SF>(v1, in_row + static_cast<int64_t>(blk_beg + 32 + lane) * SF, in_vec32);
+    int ch = c_beg + lane;  // this lane's chunks: ch, ch + 32, ...
+    if constexpr (FMT == kNVFP4) {
+      // two alternating buffers, one step of loads ahead (fewer registers,
+      // more resident warps: the better trade for the NVFP4 arithmetic)
+      uint4 va[4], vb[4];
+      if (ch < lim) band_load(va, in_row + 32 * ch, in_vec32);
 #pragma unroll 1
-    for (int blk0 = blk_beg; blk0 < blk_end; blk0 += 32) {
-      const int blk = blk0 + lane;
-      uint4 v[SF / 8];
+      for (int c0 = c_beg; c0 < c_end; c0 += 64, ch += 64) {
+        if (ch + 32 < lim) band_load(vb, in_row + 32 * (ch + 32), in_vec32);
+        band_chunk_step<FMT>(va, ch, n_chunks, c_end, out_row, scale_row, out_vec32, ns);
+        if (c0 + 32 >= c_end) break;
+        if (ch + 64 < lim) band_load(va, in_row + 32 * (ch + 64), in_vec32);
+        band_chunk_step<FMT>(vb, ch + 32, n_chunks, c_end, out_row, scale_row, out_vec32, ns);
+      }
+    } else {
+      // two steps of loads ahead
+      uint4 v0[4], v1[4];
+      if (ch < lim) band_load(v0, in_row + 32 * ch, in_vec32);
+      if (ch + 32 < lim) band_load(v1, in_row + 32 * (ch + 32), in_vec32);
+#pragma unroll 1
+      for (int c0 = c_beg; c0 < c_end; c0 += 32, ch += 32) {
+        uint4 v[4];
 #pragma unroll
-      for (int c = 0; c < SF / 8; ++c) { v[c] = v0[c]; v0[c] = v1[c]; }
-      const int nb = blk + 64;
-      if (nb < S && blk0 + 64 < blk_end) band_load<SF>(v1, in_row + static_cast<int64_t>(nb) * SF, in_vec32);
-      uint32_t sbyte = 0;
-      if (blk < S && blk < blk_end)
-        sbyte = band_block<FMT>(v, out_row + (Fmt<FMT>::OUT_BITS == 4 ? (blk * SF) >> 1 : blk * SF), out_vec32, ns);
-      // scale word of atom blk/4: byte blk%4 from lanes 4j..4j+3
-      uint32_t word = sbyte << (8 * (lane & 3));
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-      if ((lane & 3) == 0 && blk < blk_end)
-        *reinterpret_cast<uint32_t*>(scale_row + static_cast<int64_t>(blk >> 2) * 512) = word;
+        for (int c = 0; c < 4; ++c) { v[c] = v0[c]; v0[c] = v1[c]; }
+        if (ch + 64 < lim) band_load(v1, in_row + 32 * (ch + 64), in_vec32);
+        band_chunk_step<FMT>(v, ch, n_chunks, c_end, out_row, scale_row, out_vec32, ns);
+      }
     }
   }
 }
