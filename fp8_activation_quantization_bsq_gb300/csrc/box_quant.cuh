@@ -9,19 +9,16 @@
 namespace bsq {
 
 // NVFP4 element-scale source: a 256-entry table indexed by the scale byte,
-// or the 16-entry quotient table fl32(tensor_sf / j), or (both null) the
-// division tensor_sf / ds itself.
+// or (null) the division tensor_sf / ds itself.
 struct NvScale {
   float tsf;
   const float* factor_tab;  // 256 entries, or nullptr
-  const float* q16;         // 16 entries, or nullptr
   const float* div6_tab;    // 128 entries: fl32((128 + f) / 192)
 };
 
 __device__ __forceinline__ BlockScale nvfp4_block_scale(float amax, const NvScale& ns) {
   const uint32_t b = f32_to_e4m3(__fmul_rn(amax_div6(amax, ns.div6_tab), ns.tsf));
   if (ns.factor_tab) return {b, ns.factor_tab[b]};
-  if (ns.q16) return {b, nvfp4_factor_q(b, ns.tsf, ns.q16[nvfp4_q_index(b)])};
   const float ds = e4m3_to_f32(b);
   return {b, ds == 0.0f ? 0.0f : __fdiv_rn(ns.tsf, ds)};
 }

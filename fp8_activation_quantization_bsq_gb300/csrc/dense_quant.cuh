@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kDenseThreads)
   const int r4 = lane >> 3;
   const int row = r32 + 32 * r4;
   const int atom_off = r32 * 16 + r4 * 4;  // this row's word inside a 512-byte atom
-  const NvScale ns{tsf, factor_tab, nullptr, div6_tab};
+  const NvScale ns{tsf, factor_tab, div6_tab};
 
   int stage = 0;
   uint32_t phase = 0;

@@ -150,15 +150,6 @@ struct MxScale {
   uint16_t pow2;  // 2^-e as BF16 bits (exact)
 };
 
-// NVFP4: s = fl32(fl32(amax / 6) * tensor_sf) -> E4M3; element scale
-// tensor_sf / decoded scale (0 when the decoded scale is 0).
-__device__ __forceinline__ BlockScale nvfp4_scale(float amax, float tsf) {
-  const float s = __fmul_rn(__fdiv_rn(amax, 6.0f), tsf);
-  const uint32_t b = f32_to_e4m3(s);
-  const float ds = e4m3_to_f32(b);
-  return {b, ds == 0.0f ? 0.0f : __fdiv_rn(tsf, ds)};
-}
-
 // MX: e = ceil(log2(fl32(amax / Qmax))) clamped to [-127, 127] (-127 for a
 // zero block); byte e+127, element factor 2^-e.
 //
@@ -206,35 +197,6 @@ __device__ __forceinline__ float amax_div6(float amax, const float* div6_tab) {
   const uint32_t e = bits >> 23;
   if (e < 5u) return __fdiv_rn(amax, 6.0f);
   return __fmul_rn(div6_tab[(bits >> 16) & 0x7Fu], __uint_as_float((e - 2u) << 23));
-}
-
-// NVFP4 element scale from a 16-entry quotient table q[j] = fl32(tensor_sf / j)
-// (j = 1..15).  A positive E4M3 value is ds = j * 2^t with j = 8 + m, t = E - 10
-// (normal) or j = m, t = -9 (subnormal), so tensor_sf / ds = (tensor_sf / j) *
-// 2^-t and, while that result is a normal FP32 value, fl32(tensor_sf / ds) =
-// fl32(tensor_sf / j) * 2^-t exactly (scaling by a power of two commutes with
-// rounding).  Subnormal or overflowing results take the division.
-__device__ __forceinline__ float nvfp4_factor_q(uint32_t b, float tsf, float qj) {
-  if ((b & 0x7Fu) == 0u) return 0.0f;  // decoded scale 0
-  const uint32_t E = (b >> 3) & 0xFu;
-  const int t = E ? static_cast<int>(E) - 10 : -9;
-  const uint32_t qb = __float_as_uint(qj);
-  const int qe = static_cast<int>(qb >> 23);  // qj > 0: biased exponent
-  const int re = qe - t;
-  if (qe == 0 || re <= 0 || re >= 255) return __fdiv_rn(tsf, e4m3_to_f32(b));
-  return __uint_as_float(qb - (static_cast<uint32_t>(t) << 23));
-}
-__device__ __forceinline__ uint32_t nvfp4_q_index(uint32_t b) {
-  const uint32_t E = (b >> 3) & 0xFu, m = b & 7u;
-  return E ? 8u + m : m;
-}
-
-// NVFP4 block scale via the tables: s = fl32(fl32(amax / 6) * tensor_sf) -> E4M3,
-// element factor factor_tab[byte].
-__device__ __forceinline__ BlockScale nvfp4_scale_tab(float amax, float tsf, const float* factor_tab,
-                                                      const float* div6_tab) {
-  const uint32_t b = f32_to_e4m3(__fmul_rn(amax_div6(amax, div6_tab), tsf));
-  return {b, factor_tab[b]};
 }
 
 // ------------------------------------------------------------------- PTX --

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(co
     const uint16_t* in_row = a.in + row.src * a.ld_in;
     uint8_t* out_row = a.out + row.dst * a.out_ld;
     uint8_t* scale_row = a.scales + row.band + row.atom_off;
-    const NvScale ns{row.tsf, row.tab >= 0 ? factor_tab[row.tab] : nullptr, nullptr, div6_tab};
+    const NvScale ns{row.tsf, row.tab >= 0 ? factor_tab[row.tab] : nullptr, div6_tab};
     int ch = c_beg + lane;  // this lane's chunks: ch, ch + 32, ...
     if constexpr (FMT == kNVFP4) {
       // two alternating buffers, one step of loads ahead (fewer registers,
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
       uint8_t* dst = a.out + rs[r].dst * a.out_ld + (Fmt<FMT>::OUT_BITS == 4 ? col >> 1 : col);
       uint32_t sbyte;
       if constexpr (FMT == kNVFP4) {
-        const NvScale ns{rs[r].tsf, nullptr, nullptr, div6_tab};
+        const NvScale ns{rs[r].tsf, nullptr, div6_tab};
         const BlockScale sc = nvfp4_block_scale(amax, ns);
         sbyte = sc.byte;
         const uint32_t o0 = quant8_e2m1(v[u][0], sc.factor), o1 = quant8_e2m1(v[u][1], sc.factor);
