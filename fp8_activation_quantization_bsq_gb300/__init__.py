@@ -24,7 +24,7 @@ from ._build import LIB_PATH
 
 __all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes",
            "scales5d_bytes", "quantize", "quantize_dynamic", "tensor_sf", "grouped_tensor_sf",
-           "grouped_quantize", "scales_interleave", "device_error", "status_string"]
+           "grouped_quantize", "scales_interleave", "block_scaled_dot", "device_error", "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
 GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2}
@@ -54,6 +54,8 @@ _SIGNATURES = {
     "bsq_grouped_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i32,
                                        _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p]),
     "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),
+    "bsq_block_scaled_dot": (_c_i32, [_c_i32, _c_p, _c_p, ctypes.c_float, _c_p, _c_p, ctypes.c_float,
+                                      _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
 }
 
 _lib = None
@@ -258,6 +260,23 @@ def scales_interleave(scales2d: torch.Tensor, out=None, stream=None):
         rc = lib().bsq_scales_interleave(_ptr(scales2d), M, S, scales2d.stride(0) if M else S,
                                          _ptr(out), _stream(scales2d.device, stream))
     _check(rc, "bsq_scales_interleave")
+    return out
+
+
+def block_scaled_dot(fmt, a_packed: torch.Tensor, a_scales: torch.Tensor, b_packed: torch.Tensor,
+                     b_scales: torch.Tensor, K: int, a_tsf: float = 1.0, b_tsf: float = 1.0,
+                     out=None, stream=None) -> torch.Tensor:
+    """float64 (M, N) = dequantized A (M, K) times dequantized B (N, K)^T, from
+    packed rows and 5D scales (a slow FP64 validator, not a fast matmul)."""
+    f = _fmt(fmt)
+    M, N = a_packed.shape[0], b_packed.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float64, device=a_packed.device)
+    with torch.cuda.device(a_packed.device):
+        rc = lib().bsq_block_scaled_dot(f, _ptr(a_packed), _ptr(a_scales), float(a_tsf), _ptr(b_packed),
+                                        _ptr(b_scales), float(b_tsf), M, N, K, _ptr(out),
+                                        _stream(a_packed.device, stream))
+    _check(rc, "bsq_block_scaled_dot")
     return out
 
 

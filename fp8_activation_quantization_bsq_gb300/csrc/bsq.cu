@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <utility>
 
+#include "block_scaled_dot.cuh"
 #include "dense_quant.cuh"
 #include "device_common.cuh"
 #include "grouped_quant.cuh"
@@ -437,6 +438,42 @@ int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_
     e = launch_pdl(interleave_kernel<4>, grid, dim3(kIlvThreads), 0, st, in, M, S, ld, out, ikt);
   else
     e = launch_pdl(interleave_kernel<1>, grid, dim3(kIlvThreads), 0, st, in, M, S, ld, out, ikt);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed, const void* a_scales5d, float a_tsf,
+                             const void* b_packed, const void* b_scales5d, float b_tsf, int64_t M,
+                             int64_t N, int64_t K, double* c_out, void* stream) {
+  if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || K >= (int64_t(1) << 31) || M >= (int64_t(1) << 35) ||
+      N >= (int64_t(1) << 35))
+    return BSQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return BSQ_OK;
+  if (!c_out || (K > 0 && (!a_packed || !a_scales5d || !b_packed || !b_scales5d))) return BSQ_ERR_NULL;
+  if (!aligned(c_out, 8)) return BSQ_ERR_ALIGN;
+  if (fmt == BSQ_NVFP4 && !(std::isfinite(a_tsf) && a_tsf > 0.0f && std::isfinite(b_tsf) && b_tsf > 0.0f))
+    return BSQ_ERR_VALUE;
+  const double inv_tsf = fmt == BSQ_NVFP4 ? 1.0 / (static_cast<double>(a_tsf) * b_tsf) : 1.0;
+  const int64_t gx = ceil_div(N, 16), gy = ceil_div(M, 16);
+  if (gx >= (int64_t(1) << 31) || gy > 65535) return BSQ_ERR_SHAPE;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const auto* ap = static_cast<const uint8_t*>(a_packed);
+  const auto* sap = static_cast<const uint8_t*>(a_scales5d);
+  const auto* bp = static_cast<const uint8_t*>(b_packed);
+  const auto* sbp = static_cast<const uint8_t*>(b_scales5d);
+  const int k = static_cast<int>(K);
+  cudaError_t e;
+  switch (fmt) {
+    case BSQ_NVFP4:
+      e = launch_pdl(block_scaled_dot_kernel<kNVFP4>, grid, dim3(256), 0, st, ap, sap, bp, sbp, M, N, k, inv_tsf, c_out);
+      break;
+    case BSQ_MXFP4:
+      e = launch_pdl(block_scaled_dot_kernel<kMXFP4>, grid, dim3(256), 0, st, ap, sap, bp, sbp, M, N, k, inv_tsf, c_out);
+      break;
+    default:
+      e = launch_pdl(block_scaled_dot_kernel<kMXFP8>, grid, dim3(256), 0, st, ap, sap, bp, sbp, M, N, k, inv_tsf, c_out);
+  }
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 

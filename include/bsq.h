@@ -288,6 +288,24 @@ BSQ_API int32_t bsq_grouped_tensor_sf_noalloc(const void* in_dev, int64_t in_row
                                               int32_t num_experts, void* stream);
 
 /*
+ * Naive block-scaled matmul, a validator of quantized operands (the
+ * "block_scaled_quantization" module page lists such a reference matmul,
+ * naive_block_scaled_matmul; this is our GPU version of the idea):
+ *   c_dev[m*N + n] = sum_k deq(A)[m][k] * deq(B)[n][k]   (FP64, row-major M x N)
+ * with deq = decoded element * decoded block scale (/ tensor_sf for NVFP4).
+ *   a_packed_dev, b_packed_dev  packed rows of A (M x K) and B (N x K), as
+ *                 bsq_quantize writes them (K/2 or K bytes per row).
+ *   a_scales5d_dev, b_scales5d_dev  their scales in the 5D layout.
+ *   a_tsf, b_tsf  NVFP4 tensor scales (finite, > 0); ignored for MX.
+ * K % 32 == 0.  One thread per output, FP64 on the CUDA cores: slow, exact
+ * per block, meant for checks, not for throughput.
+ */
+BSQ_API int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed_dev, const void* a_scales5d_dev,
+                                     float a_tsf, const void* b_packed_dev, const void* b_scales5d_dev,
+                                     float b_tsf, int64_t M, int64_t N, int64_t K, double* c_dev,
+                                     void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *code_out receives BSQ_OK or the first device-side error recorded since the
  * last call (BSQ_ERR_VALUE, BSQ_ERR_TIMEOUT).  Returns BSQ_ERR_CUDA if the

@@ -202,3 +202,19 @@ def test_tensor_scale_validation(lib):
     assert q(0, P, 128, 256, 256, P, P, P + 2, None) == ALIGN
     assert q(1, P, 128, 48, 48, P, P, None, None) == SHAPE
     assert q(0, P, 0, 256, 256, None, None, None, None) == OK     # empty: no-op
+
+
+def test_block_scaled_dot_validation(lib):
+    f = lib.bsq_block_scaled_dot
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    assert f(3, P, P, 1.0, P, P, 1.0, 4, 4, 64, P, None) == VALUE      # format
+    assert f(0, P, P, 1.0, P, P, 1.0, 4, 4, 48, P, None) == SHAPE      # K % 32
+    assert f(0, P, P, 1.0, P, P, 1.0, -1, 4, 64, P, None) == SHAPE
+    assert f(0, P, P, 1.0, P, P, 1.0, 4, 4, 64, None, None) == NULL
+    assert f(0, None, P, 1.0, P, P, 1.0, 4, 4, 64, P, None) == NULL
+    assert f(0, P, P, 1.0, P, P, 1.0, 4, 4, 64, P + 4, None) == ALIGN
+    assert f(0, P, P, 0.0, P, P, 1.0, 4, 4, 64, P, None) == VALUE      # NVFP4 tensor scale
+    assert f(0, P, P, 1.0, P, P, 1.0, 0, 4, 64, None, None) == OK      # empty: no-op

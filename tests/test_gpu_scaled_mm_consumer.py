@@ -97,6 +97,9 @@ def test_tensor_core_product_of_quantized_operands(bsq, fmt, M, N, K):
     rel = 1e-5 if info == torch.float32 else 8e-3
     err = np.abs(c_hw - c_ref)
     assert np.all(err <= rel * mag + 1e-30), f"max err/mag {np.max(err / (mag + 1e-30)):.3g} ({info})"
+    # the GPU naive block-scaled matmul reads the same bytes the same way
+    c_val = bsq.block_scaled_dot(fmt, pa, sa, pb, sb, K, tsf_a, tsf_b).cpu().numpy()
+    assert np.all(np.abs(c_hw - c_val) <= rel * mag + 1e-30)
 
     # negative control: scales in plain row-major order are not what the
     # tensor cores read, and the product must then be far off
