@@ -253,7 +253,17 @@ def extra_workloads(bsq, device, flush, peak):
     res[f"nvfp4_dynamic_chain_M{M}_K{K}"] = {
         "us": round(mean * 1e3, 2), "note": "tensor_sf + quantize_dynamic; the input is read twice",
         "GB_s_of_quantize_bytes": round(dense_bytes("nvfp4", M, K) / (mean * 1e6), 1)}
-    del x, out, sc
+
+    # the naive block-scaled matmul validator (FP64 CUDA cores), NVFP4
+    # 512 x 512 x 7168 from the first rows of the dense workload
+    xa, xb = x[:512], x[512:1024]
+    pa, sa = bsq.quantize(xa, "nvfp4", 1.0)
+    pb, sb = bsq.quantize(xb, "nvfp4", 1.0)
+    cd = bsq.block_scaled_dot("nvfp4", pa, sa, pb, sb, K)
+    mean, _ = time_events(lambda: bsq.block_scaled_dot("nvfp4", pa, sa, pb, sb, K, out=cd), 5)
+    res["block_scaled_dot_nvfp4_512x512x7168"] = {"us": round(mean * 1e3, 1),
+                                                  "GFLOP_s_fp64": round(2 * 512 * 512 * K / (mean * 1e6), 1)}
+    del pa, sa, pb, sb, cd, x, out, sc
 
     c = wl.config_dense_mx_wide()
     x = to_dev_bf16(c["x_bits"], device)

@@ -225,6 +225,10 @@ BSQ_API int32_t bsq_quantize_dynamic(int32_t fmt, const void* in_dev, int64_t M,
  *                 workspace that was not zeroed records BSQ_ERR_VALUE in the
  *                 device error word (the outputs are then not written).  Calls
  *                 sharing one workspace must not overlap on the GPU.
+ *   The reduction reads in_dev with an L2 evict_last hint, so that a quantize
+ *   of the same tensor right after it finds much of it in L2; that quantize
+ *   (or any later read with the default policy) returns the lines to normal
+ *   priority.
  */
 BSQ_API int64_t bsq_tensor_sf_workspace_bytes(void);
 BSQ_API int32_t bsq_tensor_sf(const void* in_dev, int64_t M, int64_t K, int64_t ld_in,
