@@ -12,10 +12,12 @@
 //    searching row_offsets with all 32 lanes (rounds of 256 probes), each lane
 //    steps on to its own row's group, and the distinct expert scales of the
 //    32 rows get shared element-scale tables.  Then each warp walks its rows
-//    one at a time with its 32 lanes on 32 consecutive scale blocks of the
-//    row: gathered loads and packed stores are contiguous per instruction
-//    (whole L1 lines, not one sector per lane), two steps of loads in
-//    flight, and 4 lanes OR their scale bytes into one atom word.
+//    one at a time with its 32 lanes on 32 consecutive 32-element chunks of
+//    the row (two NVFP4 scale blocks or one MX block per lane): gathered
+//    loads and packed stores are contiguous per instruction (whole L1
+//    lines, not one sector per lane), with one (NVFP4) or two (MX) steps of
+//    loads in flight, and the lanes of one atom OR their scale bytes into
+//    its word.
 //
 //  * grouped_rows_kernel (groups of a few rows, decode).  A warp owns R
 //    consecutive destination rows and one run of k_tiles_per_block atom
@@ -73,7 +75,6 @@ __device__ __forceinline__ void check_offsets(const GroupedArgs& a) {
 // keep 6-7 blocks resident per SM).
 template <int FMT>
 __host__ __device__ constexpr int band_warps() { return 4; }
-constexpr int kBdMaxThreads = 256;
 constexpr int kBdRows = 32;        // destination rows per block
 constexpr int kBdTables = 2;       // distinct tensor scales of the band with a shared element-scale table
 
