@@ -138,17 +138,17 @@ BSQ_API int32_t bsq_quantize(int32_t fmt, const void* in_dev, int64_t M, int64_t
  *   total_rows          destination rows allocated in out_dev; the device
  *                       checks row_offsets[G] <= total_rows.
  *   total_scale_rows    5D scale rows allocated (multiple of 128); the device
- *                       checks scales_offsets[G] <= total_scale_rows.  The
- *                       launch covers total_scale_rows/128 row tiles.
+ *                       checks scales_offsets[G] <= total_scale_rows.
  *   out_dev             total_rows * packed_row_bytes bytes: row d is written
  *                       iff d belongs to a group with a non-negative expert id.
  *   scales5d_dev        bsq_scales5d_bytes(fmt, total_scale_rows, K) bytes: each
  *                       written row gets all ceil(S/4)*4 scale bytes (padding
  *                       columns 0x00); padding rows are not written.
  *   k_tiles_per_block   1, 2, 4 or 8 column tiles (64 columns for NVFP4, 128
- *                       for MX) handled by one unit of work (a warp of the
- *                       latency kernel; the streaming kernel's thread blocks
- *                       take at least 1024 columns).
+ *                       for MX) handled by one unit of work of the latency
+ *                       kernel (a warp); the streaming kernel's thread blocks
+ *                       take fixed runs of 7168 columns.  Results do not
+ *                       depend on it.
  * Device checks (error word BSQ_ERR_VALUE, the affected rows are skipped):
  * a source row index outside [0, in_rows); row_offsets[G] > total_rows;
  * scales_offsets[G] > total_scale_rows; scales_offsets[0] != 0; a group with
