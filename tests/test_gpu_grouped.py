@@ -266,3 +266,30 @@ def test_grouped_strided_input_and_16_byte_aligned_outputs(bsq, fmt, kernel):
     assert margin_intact(ofull) and margin_intact(sfull)
     assert np.all(ofull[:16].cpu().numpy() == SENTINEL) and np.all(sfull[:16].cpu().numpy() == SENTINEL)
     _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy())
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_empty_groups_and_trailing_rows(bsq, fmt, kernel):
+    """Groups with no rows between non-empty ones (row_offsets and
+    scales_offsets do not advance), a group of 129 rows (two scale tiles),
+    and destination rows beyond row_offsets[G], which no group owns and which
+    stay untouched."""
+    rng = np.random.Generator(np.random.PCG64(13))
+    m = np.array([0, 5, 0, 0, 129, 1, 0, 40, 0], np.int64)
+    G = m.size
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = np.concatenate([[0], np.cumsum(-(-m // 128) * 128)]).astype(np.uint32)
+    total_rows = int(ro[-1]) + 7                     # 7 trailing rows outside every group
+    K = 192
+    in_rows = 90
+    x = wl.dense_activations(rng, in_rows, K, "blocklognormal")
+    ridx = rng.integers(0, in_rows, size=total_rows).astype(np.int32)
+    eid = np.arange(G, dtype=np.int32) % 5
+    sf = (rng.random(5).astype(np.float32) + np.float32(0.5))
+    d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=eid, sf_tensor=sf,
+             row_indices=ridx, total_rows=total_rows, total_scale_rows=int(so[-1]), G=G)
+    p, s = _run_grouped(bsq, fmt, d, 2, kernel=kernel)
+    owned = int(ro[-1])
+    _compare(fmt, d, p[:owned], s)
+    assert np.all(p[owned:] == SENTINEL)
