@@ -54,6 +54,7 @@ _SIGNATURES = {
     "bsq_grouped_tensor_sf": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i32,
                                        _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p]),
     "bsq_device_error": (_c_i32, [_c_p, ctypes.POINTER(_c_i32)]),
+    "bsq_selftest_wait_timeout": (_c_i32, [_c_p]),
     "bsq_block_scaled_dot": (_c_i32, [_c_i32, _c_p, _c_p, ctypes.c_float, _c_p, _c_p, ctypes.c_float,
                                       _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
 }

@@ -23,6 +23,20 @@ namespace {
 
 using namespace bsq;
 
+// Self-test of the bounded waits: an mbarrier that nothing arrives on is
+// waited for with the same bounded wait the pipelined kernels use; it gives
+// up after about a second and records BSQ_ERR_TIMEOUT.
+__global__ void wait_timeout_selftest_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0)) record_error(kErrTimeout);
+}
+
 constexpr int kDenseStages = 3;
 constexpr int kMaxDevices = 64;
 // Grouped quantize: groups averaging at most kGroupedLatencyMaxAvgRows rows
@@ -474,6 +488,12 @@ int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed, const void* a_sc
     default:
       e = launch_pdl(block_scaled_dot_kernel<kMXFP8>, grid, dim3(256), 0, st, ap, sap, bp, sbp, M, N, k, inv_tsf, c_out);
   }
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+int32_t bsq_selftest_wait_timeout(void* stream) {
+  const cudaError_t e = launch_pdl(wait_timeout_selftest_kernel, dim3(1), dim3(32), 0,
+                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 

@@ -310,6 +310,15 @@ BSQ_API int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed_dev, cons
                                      void* stream);
 
 /*
+ * Self-test of the device-side failure path: enqueues a one-warp kernel that
+ * waits, with the bounded wait every pipelined kernel here uses, on a
+ * barrier nothing will complete.  After about one second the wait gives up
+ * and records BSQ_ERR_TIMEOUT in the error word (read it with
+ * bsq_device_error); nothing faults or hangs, and the context stays usable.
+ */
+BSQ_API int32_t bsq_selftest_wait_timeout(void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *code_out receives BSQ_OK or the first device-side error recorded since the
  * last call (BSQ_ERR_VALUE, BSQ_ERR_TIMEOUT).  Returns BSQ_ERR_CUDA if the
