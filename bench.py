@@ -314,6 +314,18 @@ def extra_workloads(bsq, device, flush, peak):
                                                          out=gsf, workspace=gws), reps, flush)
     res["grouped_tensor_sf_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2),
                                                     "gathered_GB_s": round(d["total_rows"] * d["K"] * 2 / (mean * 1e6), 1)}
+    # the grouped dynamic chain: per-expert scales on the GPU, then the
+    # grouped NVFP4 quantize reading them from device memory
+    so_d = torch.from_numpy(np.ascontiguousarray(d["scales_offsets"], np.uint32).view(np.int32)).to(device)
+    gkw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=8)
+    go, gsc = bsq.grouped_quantize(xg, "nvfp4", ro, so_d, eid, gsf, ridx, **gkw)
+
+    def gchain():
+        bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], out=gsf, workspace=gws)
+        bsq.grouped_quantize(xg, "nvfp4", ro, so_d, eid, gsf, ridx, out=go, scales=gsc, **gkw)
+    mean, mn = time_events(gchain, reps, flush)
+    res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2)}
+    del go, gsc, so_d
     del xg, gsf, gws
     for fmt in ("nvfp4", "mxfp8", "mxfp4"):
         mean, mn, b = grouped(d, fmt, 8, "prefill", uniq)

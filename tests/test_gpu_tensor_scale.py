@@ -160,3 +160,24 @@ def test_workspaces_left_zeroed_and_unzeroed_ones_reported(bsq):
     gbad = torch.full_like(gws, 0xFF)
     bsq.grouped_tensor_sf(*args, total_rows=d["total_rows"], workspace=gbad)
     assert bsq.device_error() == 4
+
+
+@pytest.mark.parametrize("kernel", ["stream", "latency"])
+def test_grouped_dynamic_chain_matches_oracle(bsq, kernel):
+    """Per-expert tensor scales computed on the GPU feed the grouped NVFP4
+    quantize directly (device memory, no host round trip)."""
+    d = wl.config_grouped_prefill(seed=7, tokens=160, K=512, num_experts=24, top_k=4)
+    E = 24
+    x = to_device_bf16(d["x_bits"])
+    ro, so = u32_device(d["row_offsets"]), u32_device(d["scales_offsets"])
+    eid, ridx = i32_device(d["expert_ids"]), i32_device(d["row_indices"])
+    sf = bsq.grouped_tensor_sf(x, ro, eid, E, ridx, total_rows=d["total_rows"])
+    out, sc = bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, total_rows=d["total_rows"],
+                                   total_scale_rows=d["total_scale_rows"], k_tiles_per_block=2,
+                                   kernel=kernel)
+    _, sf_ref = oracle.expert_tensor_sf(d["x_bits"], d["row_offsets"], d["expert_ids"], E, d["row_indices"])
+    p_ref, pw, s_ref, sw = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"], d["scales_offsets"],
+                                                   d["expert_ids"], sf_ref, d["row_indices"])
+    np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
+    np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
+    assert bsq.device_error() == 0
