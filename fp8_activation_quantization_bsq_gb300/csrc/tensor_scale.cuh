@@ -9,8 +9,10 @@
 // finish (fenced atomic counter) reduces the partials and writes
 // {amax, tensor_sf}.  Grouped: one warp per destination row, its group by a
 // binary search over row_offsets, an atomic max per expert (non-negative FP32
-// maxima order like their bit patterns), and the last block writes sf_tensor.
-// Both leave their workspace zeroed for the next launch.
+// maxima order like their bit patterns), and the last block writes sf_tensor;
+// when a gather reuses source rows over few tokens, a token-major variant
+// reads each source row once and scans row_indices instead.  All leave their
+// workspace zeroed for the next launch.
 #pragma once
 
 #include "device_common.cuh"
@@ -158,6 +160,178 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
     if (lane == 0 && m != 0u) atomicMax(a.amax_bits + e, m);
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int ticket = atomicAdd(a.counter, 1u);
+    if (ticket >= gridDim.x) record_error(kErrValue);
+    last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < a.num_experts; e += kAmaxThreads) {
+    a.sf[e] = tensor_sf_of(__uint_as_float(__ldcg(a.amax_bits + e)));
+    a.amax_bits[e] = 0u;  // ready for the next launch
+  }
+  if (threadIdx.x == 0) *a.counter = 0u;
+}
+
+// Per-expert maxima, token-major (a row_indices gather that reuses source
+// rows, e.g. top-k routing).  A cluster of kAtCluster blocks owns
+// kAtCluster * kAtTokens consecutive source rows: each block reduces the max
+// |x| of its kAtTokens rows once (one warp per row) into shared memory; then
+// each block of the cluster scans its contiguous share of row_indices, and
+// each destination row whose source row the cluster owns folds that row's
+// maximum (read from the owning block's shared memory) into a per-group
+// maximum in shared memory; the block then issues one atomic max per group
+// it touched.  The same maxima as grouped_amax_kernel (max is exact and
+// order-free), with each source row read once instead of once per
+// destination row, and row_indices read once per cluster, in 16-byte
+// vectors.  Metadata errors of a destination row are reported by the cluster
+// owning its source row (a source row outside x: by the first cluster), as
+// in grouped_amax_kernel.
+constexpr int kAtTokens = kAmaxWarps;
+constexpr int kAtCluster = 8;
+constexpr int kAtClusterTokens = kAtCluster * kAtTokens;
+constexpr int kAtMaxGroups = 1024;
+
+struct AtShared {
+  uint32_t ro[kAtMaxGroups + 1];
+  int32_t e[kAtMaxGroups];
+  uint32_t gmax[kAtMaxGroups];  // per-group maximum found by this block's scan
+  uint32_t rowmax[kAtTokens];
+};
+
+// max |x| over one row (K % 8 == 0): eight 16-byte loads in flight per lane,
+// the last round predicated.
+__device__ __forceinline__ uint32_t row_absmax_wide(const uint16_t* row, int K, int lane, uint64_t pol) {
+  uint32_t acc = 0;
+  const int chunks = K >> 3;
+  for (int c = lane; c < chunks; c += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      v[k] = c + 32 * k < chunks ? ld_global_nc_v4_policy(row + 8 * (c + 32 * k), pol) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc = absmax2(acc, v[k].x); acc = absmax2(acc, v[k].y);
+      acc = absmax2(acc, v[k].z); acc = absmax2(acc, v[k].w);
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// rowmax[k] of block `rank` of this cluster (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rowmax(const AtShared& sh, int rank, int k) {
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&sh.rowmax[k]));
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Destination row d gathers source row src; fold it in if this cluster owns src.
+__device__ __forceinline__ void at_visit(const GroupedAmaxArgs& a, AtShared& sh, int64_t c0,
+                                         bool first_cluster, int64_t d, int64_t src) {
+  const bool bad_src = src < 0 || src >= a.in_rows;
+  const int64_t k = src - c0;
+  if (bad_src ? !first_cluster : (k < 0 || k >= kAtClusterTokens)) return;
+  int lo = 0, hi = a.G - 1;  // g = max{g : ro[g] <= d}
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(sh.ro[mid + 1]) <= d) lo = mid + 1;
+    else hi = mid;
+  }
+  const int e = sh.e[lo];
+  if (d < static_cast<int64_t>(sh.ro[lo]) || e >= a.num_experts || (e >= 0 && bad_src)) {
+    record_error(kErrValue);
+    return;
+  }
+  if (e < 0 || bad_src) return;
+  const uint32_t m = cluster_rowmax(sh, static_cast<int>(k / kAtTokens), static_cast<int>(k % kAtTokens));
+  if (m != 0u) atomicMax(&sh.gmax[lo], m);
+}
+
+// Grid: a multiple of kAtCluster blocks covering in_rows source rows.  The
+// first batch of row_indices loads is issued before the row maxima are
+// reduced, so that the scan's L2 latency hides under the HBM reads.
+__global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThreads, 4)
+    grouped_amax_token_kernel(const GroupedAmaxArgs a) {
+  __shared__ AtShared sh;
+  __shared__ bool last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(blockIdx.x % kAtCluster);
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x / kAtCluster) * kAtClusterTokens;
+  const bool first_cluster = blockIdx.x < kAtCluster;
+  pdl_wait();
+  const int64_t ro_end = a.G > 0 ? static_cast<int64_t>(__ldg(a.row_offsets + a.G)) : 0;
+  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  // row_indices: a scalar head up to a 16-byte boundary and a scalar tail
+  // (first block of the cluster), and a 16-byte body in kAtCluster contiguous
+  // shares, one per block
+  const int64_t mis = static_cast<int64_t>(((16 - (reinterpret_cast<uintptr_t>(a.row_indices) & 15)) & 15) >> 2);
+  const int64_t head = mis < rows ? mis : rows;
+  const int64_t nvec = (rows - head) >> 2;
+  const int4* body = reinterpret_cast<const int4*>(a.row_indices + head);
+  const int64_t share = (nvec + kAtCluster - 1) / kAtCluster;
+  const int64_t vb = share * rank;
+  const int64_t ve = vb + share < nvec ? vb + share : nvec;
+  constexpr int U = 4;  // 16-byte loads in flight per thread
+  int4 q[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t v = vb + threadIdx.x + u * kAmaxThreads;
+    q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
+  }
+  for (int i = threadIdx.x; i <= a.G; i += kAmaxThreads) {
+    sh.ro[i] = __ldg(a.row_offsets + i);
+    if (i < a.G) {
+      sh.e[i] = __ldg(a.expert_ids + i);
+      sh.gmax[i] = 0u;
+    }
+  }
+  {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kAtTokens + warp;
+    uint32_t m = 0;
+    if (t < a.in_rows)
+      m = warp_max_bits(
+          __float_as_uint(absmax_final(row_absmax_wide(a.in + t * a.ld_in, a.K, lane, l2_policy_evict_last()))));
+    if (lane == 0) sh.rowmax[warp] = m;
+  }
+  __syncthreads();
+  cluster_sync_all();  // every block's rowmax is visible to the cluster
+  if (rank == 0 && threadIdx.x < head) at_visit(a, sh, c0, first_cluster, threadIdx.x, __ldg(a.row_indices + threadIdx.x));
+  for (int64_t v0 = vb; v0 < ve; v0 += static_cast<int64_t>(kAmaxThreads) * U) {
+    if (v0 > vb) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t v = v0 + threadIdx.x + u * kAmaxThreads;
+        q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + threadIdx.x + u * kAmaxThreads;
+      if (v >= ve) continue;
+      const int64_t d = head + 4 * v;
+      at_visit(a, sh, c0, first_cluster, d, q[u].x);
+      at_visit(a, sh, c0, first_cluster, d + 1, q[u].y);
+      at_visit(a, sh, c0, first_cluster, d + 2, q[u].z);
+      at_visit(a, sh, c0, first_cluster, d + 3, q[u].w);
+    }
+  }
+  if (rank == 0)
+    for (int64_t d = head + 4 * nvec + threadIdx.x; d < rows; d += kAmaxThreads)
+      at_visit(a, sh, c0, first_cluster, d, __ldg(a.row_indices + d));
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.G; i += kAmaxThreads)
+    if (sh.gmax[i] != 0u) atomicMax(a.amax_bits + sh.e[i], sh.gmax[i]);
+  __syncthreads();
+  cluster_sync_all();  // no block leaves while another may read its rowmax
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned int ticket = atomicAdd(a.counter, 1u);

@@ -66,23 +66,66 @@ def test_tensor_sf_strided_and_workspace_reuse(bsq):
     np.testing.assert_array_equal(_f32(bsq.tensor_sf(empty, workspace=ws)), [0.0, 1.0])
 
 
-@pytest.mark.parametrize("cfg", ["prefill_small", "decode", "negative_ids"])
+# Two kernels serve grouped_tensor_sf: a gather that reuses source rows over
+# few tokens (in_rows < 16 K, at most 1024 groups) reduces each token once and
+# scans row_indices; the rest reduce every destination row.  The cases below
+# reach both: "no_gather" and "tall_short_K" take the per-row kernel.
+@pytest.mark.parametrize("cfg", ["prefill_small", "decode", "negative_ids", "no_gather", "tall_short_K",
+                                 "ragged_tokens", "indices_off_16B"])
 def test_grouped_tensor_sf_exact(bsq, cfg):
+    ridx_used = True
     if cfg == "decode":
         d = wl.config_grouped_decode(K=2048)
         E = 256
+    elif cfg == "tall_short_K":
+        d = wl.config_grouped_prefill(seed=6, tokens=1100, K=64, num_experts=16, top_k=3)
+        E = 16
+    elif cfg == "ragged_tokens":                     # a partial last block of tokens
+        d = wl.config_grouped_prefill(seed=8, tokens=37, K=512, num_experts=8, top_k=5)
+        E = 8
     else:
         d = wl.config_grouped_prefill(seed=5, tokens=200, K=256, num_experts=32, top_k=4)
         E = 32
     eid = d["expert_ids"].copy()
     if cfg == "negative_ids":
         eid[::4] = -1
-    x = to_device_bf16(d["x_bits"])
-    sf = bsq.grouped_tensor_sf(x, u32_device(d["row_offsets"]), i32_device(eid), E,
-                               i32_device(d["row_indices"]), total_rows=d["total_rows"])
-    amax, ref = oracle.expert_tensor_sf(d["x_bits"], d["row_offsets"], eid, E, d["row_indices"])
+    x_bits = d["x_bits"]
+    if cfg == "no_gather":                           # destination rows are the rows of x
+        ridx_used = False
+        x_bits = wl.dense_activations(np.random.Generator(np.random.PCG64(9)), d["total_rows"], d["K"],
+                                      "rowlognormal")
+    x = to_device_bf16(x_bits)
+    ridx = d["row_indices"] if ridx_used else None
+    ridx_dev = i32_device(ridx) if ridx_used else None
+    if cfg == "indices_off_16B":                     # row_indices 4 bytes past a 16-byte boundary
+        ridx_dev = i32_device(np.concatenate([[7], ridx]).astype(np.int32))[1:]
+    sf = bsq.grouped_tensor_sf(x, u32_device(d["row_offsets"]), i32_device(eid), E, ridx_dev,
+                               total_rows=d["total_rows"])
+    amax, ref = oracle.expert_tensor_sf(x_bits, d["row_offsets"], eid, E, ridx)
     np.testing.assert_array_equal(_f32(sf), ref)
     assert bsq.device_error() == 0
+
+
+@pytest.mark.parametrize("tokens,K", [(200, 256), (1100, 64)])
+def test_grouped_tensor_sf_reports_bad_source_rows(bsq, tokens, K):
+    """A gathered source row outside x (for an expert that is kept) is
+    reported (BSQ_ERR_VALUE) and never read, in either kernel; the same row
+    in a group with expert -1 is skipped without an error."""
+    d = wl.config_grouped_prefill(seed=10, tokens=tokens, K=K, num_experts=8, top_k=2)
+    x = to_device_bf16(d["x_bits"])
+    ro, eid = d["row_offsets"], d["expert_ids"].copy()
+    g = int(np.argmax(np.diff(ro.astype(np.int64)) > 0))     # a group with rows
+    ridx = d["row_indices"].copy()
+    ridx[ro[g]] = tokens + 5
+    assert bsq.device_error() == 0
+    bsq.grouped_tensor_sf(x, u32_device(ro), i32_device(eid), 8, i32_device(ridx), total_rows=d["total_rows"])
+    assert bsq.device_error() == 4
+    eid[g] = -1
+    sf = bsq.grouped_tensor_sf(x, u32_device(ro), i32_device(eid), 8, i32_device(ridx),
+                               total_rows=d["total_rows"])
+    assert bsq.device_error() == 0
+    _, ref = oracle.expert_tensor_sf(d["x_bits"], ro, eid, 8, ridx)
+    np.testing.assert_array_equal(_f32(sf), ref)
 
 
 def test_grouped_tensor_sf_no_groups_gives_ones(bsq):
