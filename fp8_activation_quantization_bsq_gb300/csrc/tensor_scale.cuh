@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
 // vectors.  Metadata errors of a destination row are reported by the cluster
 // owning its source row (a source row outside x: by the first cluster), as
 // in grouped_amax_kernel.
-constexpr int kAtTokens = kAmaxWarps;
+constexpr int kAtThreads = 512;
+constexpr int kAtTokens = kAtThreads / 32;
 constexpr int kAtCluster = 8;
 constexpr int kAtClusterTokens = kAtCluster * kAtTokens;
 constexpr int kAtMaxGroups = 1024;
@@ -259,7 +260,7 @@ __device__ __forceinline__ void at_visit(const GroupedAmaxArgs& a, AtShared& sh,
 // Grid: a multiple of kAtCluster blocks covering in_rows source rows.  The
 // first batch of row_indices loads is issued before the row maxima are
 // reduced, so that the scan's L2 latency hides under the HBM reads.
-__global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThreads, 4)
+__global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAtThreads, 2)
     grouped_amax_token_kernel(const GroupedAmaxArgs a) {
   __shared__ AtShared sh;
   __shared__ bool last;
@@ -280,14 +281,14 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThread
   const int64_t share = (nvec + kAtCluster - 1) / kAtCluster;
   const int64_t vb = share * rank;
   const int64_t ve = vb + share < nvec ? vb + share : nvec;
-  constexpr int U = 4;  // 16-byte loads in flight per thread
+  constexpr int U = 2;  // 16-byte loads in flight per thread
   int4 q[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int64_t v = vb + threadIdx.x + u * kAmaxThreads;
+    const int64_t v = vb + threadIdx.x + u * kAtThreads;
     q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
   }
-  for (int i = threadIdx.x; i <= a.G; i += kAmaxThreads) {
+  for (int i = threadIdx.x; i <= a.G; i += kAtThreads) {
     sh.ro[i] = __ldg(a.row_offsets + i);
     if (i < a.G) {
       sh.e[i] = __ldg(a.expert_ids + i);
@@ -305,17 +306,17 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThread
   __syncthreads();
   cluster_sync_all();  // every block's rowmax is visible to the cluster
   if (rank == 0 && threadIdx.x < head) at_visit(a, sh, c0, first_cluster, threadIdx.x, __ldg(a.row_indices + threadIdx.x));
-  for (int64_t v0 = vb; v0 < ve; v0 += static_cast<int64_t>(kAmaxThreads) * U) {
+  for (int64_t v0 = vb; v0 < ve; v0 += static_cast<int64_t>(kAtThreads) * U) {
     if (v0 > vb) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t v = v0 + threadIdx.x + u * kAmaxThreads;
+        const int64_t v = v0 + threadIdx.x + u * kAtThreads;
         q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t v = v0 + threadIdx.x + u * kAmaxThreads;
+      const int64_t v = v0 + threadIdx.x + u * kAtThreads;
       if (v >= ve) continue;
       const int64_t d = head + 4 * v;
       at_visit(a, sh, c0, first_cluster, d, q[u].x);
@@ -325,10 +326,10 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThread
     }
   }
   if (rank == 0)
-    for (int64_t d = head + 4 * nvec + threadIdx.x; d < rows; d += kAmaxThreads)
+    for (int64_t d = head + 4 * nvec + threadIdx.x; d < rows; d += kAtThreads)
       at_visit(a, sh, c0, first_cluster, d, __ldg(a.row_indices + d));
   __syncthreads();
-  for (int i = threadIdx.x; i < a.G; i += kAmaxThreads)
+  for (int i = threadIdx.x; i < a.G; i += kAtThreads)
     if (sh.gmax[i] != 0u) atomicMax(a.amax_bits + sh.e[i], sh.gmax[i]);
   __syncthreads();
   cluster_sync_all();  // no block leaves while another may read its rowmax
@@ -341,7 +342,7 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAmaxThread
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int e = threadIdx.x; e < a.num_experts; e += kAmaxThreads) {
+  for (int e = threadIdx.x; e < a.num_experts; e += kAtThreads) {
     a.sf[e] = tensor_sf_of(__uint_as_float(__ldcg(a.amax_bits + e)));
     a.amax_bits[e] = 0u;  // ready for the next launch
   }
