@@ -614,8 +614,9 @@ def run_case(args):
             fn = lambda: bsq.grouped_tensor_sf(x, ro, eid, d["num_experts"], ridx, total_rows=d["total_rows"],
                                                out=out, workspace=ws)
         else:
-            out, sc = bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, **kw)
-            fn = lambda: bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
+            kw["kernel"] = args.grouped_kernel
+            out, sc = bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, **kw)
+            fn = lambda: bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
     elif args.case == "tensor_sf":
         x = to_dev_bf16(wl.config_dense_nvfp4_large()["x_bits"], device)
         ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
@@ -651,6 +652,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the context workloads")
+    ap.add_argument("--grouped-kernel", choices=("auto", "stream", "latency", "token"), default="auto",
+                    help="kernel of the grouped --case workloads")
+    ap.add_argument("--fmt", choices=("nvfp4", "mxfp4", "mxfp8"), default="nvfp4",
+                    help="format of the grouped --case workloads")
     ap.add_argument("--case", choices=CASES, default=None,
                     help="time one context workload alone on GPU 0 (for profiling) and exit")
     args = ap.parse_args(argv)

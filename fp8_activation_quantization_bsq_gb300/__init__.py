@@ -27,7 +27,7 @@ __all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packe
            "grouped_quantize", "scales_interleave", "block_scaled_dot", "device_error", "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
-GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2}
+GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2, "token": 3}
 
 _c_i32, _c_i64, _c_f32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 

@@ -194,9 +194,31 @@ bsq_status launch_grouped_band(GroupedArgs a, cudaStream_t stream) {
 }
 
 template <int FMT>
+bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
+  // source rows the clusters own: with no row_indices every destination row
+  // is its own source row, and rows past in_rows still need their checks
+  int64_t n_tok = a.row_indices != nullptr ? a.in_rows : std::max(a.in_rows, a.total_rows);
+  n_tok = std::max<int64_t>(n_tok, 1);  // one cluster reports bad source rows
+  const int64_t blocks = ceil_div(n_tok, kTkClusterTokens) * kTkCluster;
+  if (blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  const cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)),
+                                   dim3(kTkThreads), 0, stream, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+template <int FMT>
 bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t stream) {
-  if (kernel == BSQ_GROUPED_AUTO)
-    kernel = a.total_rows <= kGroupedLatencyMaxAvgRows * a.G ? BSQ_GROUPED_LATENCY : BSQ_GROUPED_STREAM;
+  if (kernel == BSQ_GROUPED_AUTO) {
+    if (a.total_rows <= kGroupedLatencyMaxAvgRows * a.G)
+      kernel = BSQ_GROUPED_LATENCY;
+    else if (a.row_indices != nullptr && a.G <= kTkMaxGroups && a.total_rows >= 2 * a.in_rows &&
+             a.in_rows <= 64 * static_cast<int64_t>(a.K))
+      kernel = BSQ_GROUPED_TOKEN;  // source rows reused: read each once (scan cost in_rows * total_rows / 32 B)
+    else
+      kernel = BSQ_GROUPED_STREAM;
+  }
+  if (kernel == BSQ_GROUPED_TOKEN && a.G > kTkMaxGroups) kernel = BSQ_GROUPED_STREAM;
+  if (kernel == BSQ_GROUPED_TOKEN) return launch_grouped_token<FMT>(a, stream);
   if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_band<FMT>(a, stream);
   switch (kt) {
     case 1: return launch_grouped_rows<FMT, 1>(a, stream);
@@ -384,7 +406,8 @@ int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows
   if (k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
       k_tiles_per_block != 8)
     return BSQ_ERR_VALUE;
-  if (kernel != BSQ_GROUPED_AUTO && kernel != BSQ_GROUPED_STREAM && kernel != BSQ_GROUPED_LATENCY)
+  if (kernel != BSQ_GROUPED_AUTO && kernel != BSQ_GROUPED_STREAM && kernel != BSQ_GROUPED_LATENCY &&
+      kernel != BSQ_GROUPED_TOKEN)
     return BSQ_ERR_VALUE;
   if (G < 0 || G > (1 << 20)) return BSQ_ERR_VALUE;
   if (in_rows < 0 || K < 0 || K % 32 != 0 || K >= (int64_t(1) << 31) || total_rows < 0 ||

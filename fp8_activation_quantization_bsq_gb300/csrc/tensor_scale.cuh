@@ -15,6 +15,7 @@
 // workspace zeroed for the next launch.
 #pragma once
 
+#include "cluster.cuh"
 #include "device_common.cuh"
 
 namespace bsq {
@@ -222,17 +223,9 @@ __device__ __forceinline__ uint32_t row_absmax_wide(const uint16_t* row, int K, 
   return acc;
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // rowmax[k] of block `rank` of this cluster (distributed shared memory).
 __device__ __forceinline__ uint32_t cluster_rowmax(const AtShared& sh, int rank, int k) {
-  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&sh.rowmax[k]));
-  uint32_t remote, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
+  return cluster_ld_u32(cluster_map(&sh.rowmax[k], rank));
 }
 
 // Destination row d gathers source row src; fold it in if this cluster owns src.

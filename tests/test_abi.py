@@ -158,8 +158,8 @@ def test_grouped_kernel_choice_validation(lib):
     def call(kernel, out=P):
         return lib.bsq_grouped_quantize_kernel(0, P, 64, 256, 256, P, P, P, P, 8, None, 4, 64, 512,
                                                out, P, 1, kernel, None)
-    assert call(3) == VALUE and call(-1) == VALUE
-    for k in (0, 1, 2):
+    assert call(4, out=None) == VALUE and call(-1, out=None) == VALUE
+    for k in (0, 1, 2, 3):
         assert call(k, out=None) == NULL      # valid choice: stops at the next check
 
 

@@ -63,7 +63,7 @@ def _compare(fmt, d, p, s, use_ridx=True, expert_ids=None, x_bits=None, ridx=Non
     assert np.all(s[~sw] == SENTINEL), "padding scale rows were written"
 
 
-KERNELS = ["stream", "latency"]
+KERNELS = ["stream", "latency", "token"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -160,7 +160,7 @@ def test_grouped_decode_full_config(bsq, fmt, K, kt, kernel):
     _compare(fmt, d, p, s)
 
 
-@pytest.mark.parametrize("kernel", ["auto", "latency"])
+@pytest.mark.parametrize("kernel", ["auto", "latency", "stream", "token"])
 def test_grouped_prefill_full_config_sampled(bsq, kernel):
     """Prefill: 4096 tokens, top-8 over 256 experts, K=7168 (32768 rows) at
     the benchmark's launch configuration; the oracle checks sampled groups
@@ -293,3 +293,43 @@ def test_grouped_empty_groups_and_trailing_rows(bsq, fmt, kernel):
     owned = int(ro[-1])
     _compare(fmt, d, p[:owned], s)
     assert np.all(p[owned:] == SENTINEL)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_grouped_token_split_scan_head_and_tail(bsq, fmt, offset):
+    """The token-major kernel's scan of row_indices, split between the blocks
+    of each cluster: 701 tokens (six clusters of source rows), 2103
+    destination rows (not a multiple of 4) and row_indices starting 0, 4 or
+    12 bytes past a 16-byte boundary (the scalar head and tail around the
+    16-byte body); then two bad source rows, reported once and left
+    unwritten, with every other row still exact."""
+    d = wl.config_grouped_prefill(seed=20 + offset, tokens=701, K=192, num_experts=20, top_k=3, fmt=fmt)
+    K, total_rows, tsr = d["K"], d["total_rows"], d["total_scale_rows"]
+    assert total_rows % 4 != 0
+    sf = torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None
+    for bad in (False, True):
+        ridx = d["row_indices"].copy()
+        if bad:
+            ridx[5], ridx[total_rows - 1] = 701, -3
+        padded = i32_device(np.concatenate([np.full(offset, 7, np.int32), ridx]))
+        rdev = padded[offset:]
+        assert rdev.data_ptr() % 16 == 4 * offset
+        ofull, out = guarded(total_rows * oracle.packed_row_bytes(fmt, K))
+        sfull, sc = guarded(oracle.scales5d_bytes(tsr, K // oracle.block_size(fmt)))
+        bsq.grouped_quantize(to_device_bf16(d["x_bits"]), fmt, u32_device(d["row_offsets"]),
+                             u32_device(d["scales_offsets"]), i32_device(d["expert_ids"]), sf, rdev,
+                             total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=1,
+                             out=out, scales=sc, kernel="token")
+        assert bsq.device_error() == (4 if bad else 0)
+        assert margin_intact(ofull) and margin_intact(sfull)
+        p = out.cpu().numpy().reshape(total_rows, -1)
+        ok = np.ones(total_rows, bool)
+        if bad:
+            ok[[5, total_rows - 1]] = False
+            assert np.all(p[~ok] == SENTINEL)
+        p_ref, pw, s_ref, sw = oracle.grouped_quantize(fmt, d["x_bits"], d["row_offsets"], d["scales_offsets"],
+                                                       d["expert_ids"], d["sf_tensor"], d["row_indices"])
+        np.testing.assert_array_equal(p[pw & ok], p_ref[pw & ok])
+        if not bad:
+            np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
