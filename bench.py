@@ -263,7 +263,22 @@ def extra_workloads(bsq, device, flush, peak):
     mean, _ = time_events(lambda: bsq.block_scaled_dot("nvfp4", pa, sa, pb, sb, K, out=cd), 5)
     res["block_scaled_dot_nvfp4_512x512x7168"] = {"us": round(mean * 1e3, 1),
                                                   "GFLOP_s_fp64": round(2 * 512 * 512 * K / (mean * 1e6), 1)}
-    del pa, sa, pb, sb, cd, x, out, sc
+    del pa, sa, pb, sb, cd
+
+    # the quantize fused into a matmul epilogue: C (8192 x 2048) = x (8192 x
+    # 7168) times 2048 rows of x as the weight, NVFP4, against the separate
+    # quantize of the same BF16 C
+    wgt = x[4096:6144]
+    cb = torch.empty((M, 2048), dtype=torch.bfloat16, device=device)
+    gq, gs = bsq.gemm_quantize(x, wgt, "nvfp4", 1.0, c_out=cb)
+    mean, _ = time_events(lambda: bsq.gemm_quantize(x, wgt, "nvfp4", 1.0, out=gq, scales=gs), 5, flush)
+    qa, qs = bsq.quantize(cb, "nvfp4", 1.0)
+    qmean, _ = time_events(lambda: bsq.quantize(cb, "nvfp4", 1.0, out=qa, scales=qs), reps, flush)
+    res["nvfp4_gemm_quantize_epilogue_8192x2048x7168"] = {
+        "us": round(mean * 1e3, 1), "TFLOP_s_bf16_mma_sync": round(2 * M * 2048 * K / (mean * 1e9), 1),
+        "separate_quantize_of_C_us": round(qmean * 1e3, 2),
+        "note": "mma.sync mainloop; the epilogue replaces a BF16 C store plus a quantize pass"}
+    del gq, gs, qa, qs, cb, wgt, x, out, sc
 
     c = wl.config_dense_mx_wide()
     x = to_dev_bf16(c["x_bits"], device)

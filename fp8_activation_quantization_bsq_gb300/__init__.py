@@ -24,7 +24,8 @@ from ._build import LIB_PATH
 
 __all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes",
            "scales5d_bytes", "quantize", "quantize_dynamic", "tensor_sf", "grouped_tensor_sf",
-           "grouped_quantize", "scales_interleave", "block_scaled_dot", "device_error", "status_string"]
+           "grouped_quantize", "scales_interleave", "block_scaled_dot", "gemm_quantize", "device_error",
+           "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
 GROUPED_KERNELS = {"auto": 0, "stream": 1, "latency": 2, "token": 3}
@@ -57,6 +58,8 @@ _SIGNATURES = {
     "bsq_selftest_wait_timeout": (_c_i32, [_c_p]),
     "bsq_block_scaled_dot": (_c_i32, [_c_i32, _c_p, _c_p, ctypes.c_float, _c_p, _c_p, ctypes.c_float,
                                       _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
+    "bsq_gemm_quantize": (_c_i32, [_c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_f32,
+                                   _c_p, _c_p, _c_p, _c_p]),
 }
 
 _lib = None
@@ -279,6 +282,36 @@ def block_scaled_dot(fmt, a_packed: torch.Tensor, a_scales: torch.Tensor, b_pack
                                         _stream(a_packed.device, stream))
     _check(rc, "bsq_block_scaled_dot")
     return out
+
+
+def gemm_quantize(a: torch.Tensor, b: torch.Tensor, fmt, tensor_sf: float = 1.0, out=None, scales=None,
+                  c_out=None, stream=None):
+    """C = a (M, K) @ b (N, K)^T in BF16 with FP32 accumulation, quantized in
+    the matmul's epilogue: returns (packed uint8 (M, packed_row_bytes(N)),
+    scales uint8 [scales5d_bytes(M, N)]) as ``quantize`` would give for the
+    BF16 C, which is not stored unless ``c_out`` (a (M, N) bfloat16 CUDA
+    tensor) is given.  N % 128 == 0, K % 32 == 0."""
+    for t in (a, b):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError("a and b must be 2-D bfloat16 CUDA tensors with unit inner stride")
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("a and b must have the same K")
+    f = _fmt(fmt)
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, packed_row_bytes(f, N)), dtype=torch.uint8, device=a.device)
+    if scales is None:
+        scales = torch.empty(scales5d_bytes(f, M, N), dtype=torch.uint8, device=a.device)
+    if c_out is not None and (c_out.dtype != torch.bfloat16 or tuple(c_out.shape) != (M, N) or
+                              not c_out.is_contiguous()):
+        raise ValueError("c_out must be a contiguous (M, N) bfloat16 tensor")
+    with torch.cuda.device(a.device):
+        rc = lib().bsq_gemm_quantize(f, _ptr(a), _ptr(b), M, N, K, a.stride(0) if M else K,
+                                     b.stride(0) if N else K, float(tensor_sf), _ptr(out), _ptr(scales),
+                                     _ptr(c_out), _stream(a.device, stream))
+    _check(rc, "bsq_gemm_quantize")
+    return out, scales
 
 
 def device_error(device=None, stream=None) -> int:

@@ -14,6 +14,7 @@
 
 #include "block_scaled_dot.cuh"
 #include "dense_quant.cuh"
+#include "gemm_quant.cuh"
 #include "device_common.cuh"
 #include "grouped_quant.cuh"
 #include "interleave.cuh"
@@ -203,6 +204,15 @@ bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
   if (blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   const cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)),
                                    dim3(kTkThreads), 0, stream, a);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+template <int FMT>
+bsq_status launch_gemm_quant(const GemmQuantArgs& p, cudaStream_t stream) {
+  const int64_t gy = 2 * ceil_div(p.M, 128);  // every row of the last 128-row band gets its scales
+  if (gy > 65535) return BSQ_ERR_SHAPE;
+  const dim3 grid(static_cast<unsigned>(p.N / kGqBN), static_cast<unsigned>(gy));
+  const cudaError_t e = launch_pdl(gemm_quant_kernel<FMT>, grid, dim3(kGqThreads), 0, stream, p);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -462,6 +472,43 @@ int32_t bsq_grouped_quantize(int32_t fmt, const void* in, int64_t in_rows, int64
                                      expert_ids, sf, num_experts, row_indices, G, total_rows,
                                      total_scale_rows, out, scales, k_tiles_per_block,
                                      BSQ_GROUPED_AUTO, stream);
+}
+
+int32_t bsq_gemm_quantize(int32_t fmt, const void* a, const void* b, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, float tensor_sf, void* out, void* scales5d, void* c_bf16,
+                          void* stream) {
+  if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
+  if (M < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 32 != 0 || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31))
+    return BSQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return BSQ_OK;
+  if (K == 0 || lda < K || ldb < K) return BSQ_ERR_SHAPE;
+  if (!a || !b || !out || !scales5d) return BSQ_ERR_NULL;
+  if (!aligned(a, 16) || !aligned(b, 16) || lda % 8 != 0 || ldb % 8 != 0 || !aligned(out, 16) ||
+      !aligned(scales5d, 16) || !aligned(c_bf16, 16))
+    return BSQ_ERR_ALIGN;
+  if (fmt == BSQ_NVFP4 && !(std::isfinite(tensor_sf) && tensor_sf > 0.0f)) return BSQ_ERR_VALUE;
+  GemmQuantArgs p{};
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.M = M;
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.lda = lda;
+  p.ldb = ldb;
+  p.tsf = fmt == BSQ_NVFP4 ? tensor_sf : 1.0f;
+  p.out = static_cast<uint8_t*>(out);
+  p.out_ld = row_bytes_of(fmt, N);
+  p.scales = static_cast<uint8_t*>(scales5d);
+  p.kt_atoms = static_cast<int>(N / atom_cols_of(fmt));
+  p.c = static_cast<uint16_t*>(c_bf16);
+  p.vec32 = aligned(out, 32) && p.out_ld % 32 == 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (fmt) {
+    case BSQ_NVFP4: return launch_gemm_quant<kNVFP4>(p, st);
+    case BSQ_MXFP4: return launch_gemm_quant<kMXFP4>(p, st);
+    default: return launch_gemm_quant<kMXFP8>(p, st);
+  }
 }
 
 int32_t bsq_scales_interleave(const void* scales2d, int64_t M, int64_t S, int64_t ld,

@@ -315,6 +315,34 @@ BSQ_API int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed_dev, cons
                                      void* stream);
 
 /*
+ * A producer with the quantize fused into its epilogue: C = A * B^T with BF16
+ * operands and FP32 accumulation, C rounded to BF16 (round to nearest even)
+ * and quantized block-wise along N exactly as bsq_quantize quantizes a BF16
+ * M x N tensor, without storing C.  The block_scaled_quantization module page
+ * (function list, block_scaled_matmul_with_epilogue) runs the elementwise
+ * epilogues of its block-scaled matmul as a separate kernel; this is the
+ * fused form for the quantize.
+ *   a_dev         M rows of K BF16 values, row stride lda elements (lda >= K,
+ *                 lda % 8 == 0, 16-byte aligned).
+ *   b_dev         N rows of K BF16 values (the weight, K-major), row stride
+ *                 ldb (ldb >= K, ldb % 8 == 0, 16-byte aligned).
+ *   M, N, K       M >= 0 (0 = no-op), N % 128 == 0, K % 32 == 0, K > 0.
+ *   tensor_sf     NVFP4 tensor scale (finite, > 0); ignored for MX.
+ *   out_dev       M x bsq_packed_row_bytes(fmt, N) packed codes, 16-byte aligned.
+ *   scales5d_dev  bsq_scales5d_bytes(fmt, M, N) bytes of 5D scales, all
+ *                 written (rows past M in the last 128-row band: 0x00).
+ *   c_bf16_dev    optional (NULL = none): M x N BF16 copy of C, row stride N,
+ *                 16-byte aligned (for checks: the fused bytes equal
+ *                 bsq_quantize applied to it).
+ * The mainloop is the warp-level tensor-core path (mma.sync), 64 x 64 tiles;
+ * errors: BSQ_ERR_SHAPE, BSQ_ERR_NULL, BSQ_ERR_ALIGN, BSQ_ERR_VALUE (format or
+ * tensor_sf), BSQ_ERR_CUDA (launch).
+ */
+BSQ_API int32_t bsq_gemm_quantize(int32_t fmt, const void* a_dev, const void* b_dev, int64_t M, int64_t N,
+                                  int64_t K, int64_t lda, int64_t ldb, float tensor_sf, void* out_dev,
+                                  void* scales5d_dev, void* c_bf16_dev, void* stream);
+
+/*
  * Self-test of the device-side failure path: enqueues a one-warp kernel that
  * waits, with the bounded wait every pipelined kernel here uses, on a
  * barrier nothing will complete.  After about one second the wait gives up

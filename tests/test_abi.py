@@ -218,3 +218,32 @@ def test_block_scaled_dot_validation(lib):
     assert f(0, P, P, 1.0, P, P, 1.0, 4, 4, 64, P + 4, None) == ALIGN
     assert f(0, P, P, 0.0, P, P, 1.0, 4, 4, 64, P, None) == VALUE      # NVFP4 tensor scale
     assert f(0, P, P, 1.0, P, P, 1.0, 0, 4, 64, None, None) == OK      # empty: no-op
+
+
+def test_gemm_quantize_validation(lib):
+    """Every rejected call returns before anything is enqueued (no valid
+    call is made with the fake pointer)."""
+    f = lib.bsq_gemm_quantize
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+
+    def call(fmt=1, a=P, b=P, M=64, N=128, K=64, lda=64, ldb=64, tsf=1.0, out=P, sc=P, c=None):
+        return f(fmt, a, b, M, N, K, lda, ldb, tsf, out, sc, c, None)
+    assert call(fmt=3, out=None) == VALUE
+    assert call(N=192, out=None) == SHAPE           # N % 128
+    assert call(K=48, lda=48, ldb=48, out=None) == SHAPE   # K % 32
+    assert call(M=-1, out=None) == SHAPE
+    assert call(K=0, lda=0, ldb=0, out=None) == SHAPE
+    assert call(lda=32, out=None) == SHAPE          # lda < K
+    assert call(a=None) == NULL
+    assert call(out=None) == NULL
+    assert call(sc=None) == NULL
+    assert call(a=P + 2) == ALIGN
+    assert call(K=32, lda=36, ldb=32) == ALIGN      # lda % 8
+    assert call(c=P + 4) == ALIGN
+    assert call(fmt=0, tsf=0.0) == VALUE            # NVFP4 tensor scale
+    assert call(fmt=0, tsf=float("inf")) == VALUE
+    assert call(M=0, a=None, b=None, out=None, sc=None) == OK   # empty: no-op
+

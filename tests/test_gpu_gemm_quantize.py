@@ -1,0 +1,65 @@
+"""GPU check of the quantize fused into a matmul epilogue (bsq_gemm_quantize):
+C = A B^T with BF16 operands and FP32 accumulation, rounded to BF16 and
+quantized without being stored.
+
+Two pins, each independent of the kernel: the packed bytes and 5D scales
+equal the oracle's quantization of the kernel's own BF16 C (bit for bit, all
+scale bytes including the zero padding rows), and that BF16 C equals the
+FP64 product within the FP32-accumulation and BF16-rounding bound.  The
+fused call without the C copy gives the same bytes."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from bsq_testlib import to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    import fp8_activation_quantization_bsq_gb300 as m
+    from fp8_activation_quantization_bsq_gb300 import _build
+    _build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("M,N,K,lda_pad", [(128, 128, 64, 0), (200, 256, 96, 8), (1, 128, 32, 0),
+                                           (333, 384, 160, 16), (64, 512, 1024, 0)])
+def test_fused_epilogue_equals_quantize_of_its_bf16_product(bsq, fmt, M, N, K, lda_pad):
+    rng = np.random.Generator(np.random.PCG64(M + N + K))
+    a_bits = wl.dense_activations(rng, M, K + lda_pad, "rowlognormal")
+    b_bits = wl.dense_activations(rng, N, K, "normal")
+    a = to_device_bf16(a_bits)[:, :K]                  # row stride K + lda_pad
+    b = to_device_bf16(b_bits)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    # tensor scale of C from a first pass (delayed scaling), then the checked call
+    bsq.gemm_quantize(a, b, fmt, 1.0, c_out=c)
+    c_bits = c.view(torch.int16).cpu().numpy().view(np.uint16)
+    tsf = float(oracle.tensor_sf(c_bits)[1]) if fmt == "nvfp4" else 1.0
+    out, sc = bsq.gemm_quantize(a, b, fmt, tsf, c_out=c)
+    c_bits = c.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert bsq.device_error() == 0
+    # (1) the epilogue is the quantize of the BF16 product
+    p_ref, s_ref = oracle.quantize(fmt, c_bits, tsf)
+    np.testing.assert_array_equal(out.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(sc.cpu().numpy(), s_ref)
+    # (2) the BF16 product against FP64
+    a64 = _bf16_to_f64(a_bits[:, :K])
+    b64 = _bf16_to_f64(b_bits)
+    c64 = a64 @ b64.T
+    mag = np.abs(a64) @ np.abs(b64).T
+    err = np.abs(_bf16_to_f64(c_bits) - c64)
+    assert np.all(err <= 2.0 ** -8 * np.abs(c64) + K * 2.0 ** -23 * mag + 1e-30)
+    # (3) the fused call without storing C gives the same bytes
+    out2, sc2 = bsq.gemm_quantize(a, b, fmt, tsf)
+    assert torch.equal(out2, out) and torch.equal(sc2, sc)
