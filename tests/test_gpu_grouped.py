@@ -333,3 +333,18 @@ def test_grouped_token_split_scan_head_and_tail(bsq, fmt, offset):
         np.testing.assert_array_equal(p[pw & ok], p_ref[pw & ok])
         if not bad:
             np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_grouped_nvfp4_extreme_tensor_scales(bsq, kernel):
+    """NVFP4 tensor scales at and beyond the range where the token kernel's
+    per-row factor table is exact (2^-117 .. 2^118; outside it the kernel
+    divides): tiny, huge and boundary values, one per expert, every kernel
+    bit-exact against the oracle."""
+    d = wl.config_grouped_prefill(seed=31, tokens=150, K=256, num_experts=10, top_k=3)
+    sf = np.array([1e-37, 2.0 ** -117, 2.0 ** -118, 3e36, 2.0 ** 118, 2.0 ** 119, 6e-36, 1.0, 1e-44, 3.4e38],
+                  np.float32)
+    d = dict(d, sf_tensor=sf[:10])
+    p, s = _run_grouped(bsq, "nvfp4", d, 2, kernel=kernel)
+    _compare("nvfp4", d, p, s)
+
