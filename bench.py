@@ -600,7 +600,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-CASES = ("grouped_prefill", "grouped_decode", "tensor_sf", "grouped_tensor_sf", "mxfp8", "mxfp4")
+CASES = ("grouped_prefill", "grouped_decode", "tensor_sf", "grouped_tensor_sf", "mxfp8", "mxfp4", "gemm_quantize")
 
 
 def run_case(args):
@@ -632,6 +632,12 @@ def run_case(args):
             kw["kernel"] = args.grouped_kernel
             out, sc = bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, **kw)
             fn = lambda: bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
+    elif args.case == "gemm_quantize":
+        # NVFP4 quantize fused into the epilogue of 8192 x 2048 x 7168
+        x = to_dev_bf16(wl.config_dense_nvfp4_large()["x_bits"], device)
+        wgt = x[4096:6144]
+        out, sc = bsq.gemm_quantize(x, wgt, "nvfp4", 1.0)
+        fn = lambda: bsq.gemm_quantize(x, wgt, "nvfp4", 1.0, out=out, scales=sc)
     elif args.case == "tensor_sf":
         x = to_dev_bf16(wl.config_dense_nvfp4_large()["x_bits"], device)
         ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
