@@ -222,8 +222,11 @@ bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t
     if (a.total_rows <= kGroupedLatencyMaxAvgRows * a.G)
       kernel = BSQ_GROUPED_LATENCY;
     else if (a.row_indices != nullptr && a.G <= kTkMaxGroups && a.total_rows >= 2 * a.in_rows &&
-             a.in_rows <= 64 * static_cast<int64_t>(a.K))
-      kernel = BSQ_GROUPED_TOKEN;  // source rows reused: read each once (scan cost in_rows * total_rows / 32 B)
+             a.in_rows <= 8 * static_cast<int64_t>(a.K))
+      // source rows reused: read each once.  The clusters' scans read
+      // in_rows * total_rows / 32 bytes of row_indices, in_rows / (64 K) of
+      // the gathered row bytes: kept to at most an eighth.
+      kernel = BSQ_GROUPED_TOKEN;
     else
       kernel = BSQ_GROUPED_STREAM;
   }

@@ -165,7 +165,7 @@ BSQ_API int32_t bsq_grouped_quantize(int32_t fmt, const void* in_dev, int64_t in
 /* Kernel of the grouped quantize. */
 typedef enum {
   BSQ_GROUPED_AUTO = 0,    /* LATENCY when total_rows <= 16 * G; else TOKEN when row_indices is
-                              given, G <= 1024, total_rows >= 2 * in_rows and in_rows <= 64 * K;
+                              given, G <= 1024, total_rows >= 2 * in_rows and in_rows <= 8 * K;
                               else STREAM */
   BSQ_GROUPED_STREAM = 1,  /* one thread block per 32 destination rows x a run of scale blocks,
                               a warp per row at a time (groups of many rows) */
