@@ -390,10 +390,11 @@ int32_t bsq_grouped_tensor_sf(const void* in, int64_t in_rows, int64_t K, int64_
   a.sf = sf_out;
   // A gather that reuses source rows (row_indices, several destination rows
   // per source row): reduce each source row once, token-major, as long as
-  // scanning row_indices once per 128 source rows costs well below reading the
-  // gathered rows (in_rows < 16 K) and the group metadata fits in shared memory.
+  // scanning row_indices once per 128 source rows stays under an eighth of
+  // the gathered row bytes (in_rows <= 8 K) and the group metadata fits in
+  // shared memory.
   const int64_t at_blocks = ceil_div(in_rows, kAtClusterTokens) * kAtCluster;
-  if (row_indices != nullptr && G <= kAtMaxGroups && a.total_rows > in_rows && in_rows < 16 * K &&
+  if (row_indices != nullptr && G <= kAtMaxGroups && a.total_rows > in_rows && in_rows <= 8 * K &&
       in_rows > 0 && at_blocks < (int64_t(1) << 31)) {
     const int64_t blocks = at_blocks;
     const cudaError_t e = launch_pdl(grouped_amax_token_kernel, dim3(static_cast<unsigned>(blocks)),

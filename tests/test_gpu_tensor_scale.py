@@ -67,7 +67,7 @@ def test_tensor_sf_strided_and_workspace_reuse(bsq):
 
 
 # Two kernels serve grouped_tensor_sf: a gather that reuses source rows over
-# few tokens (in_rows < 16 K, at most 1024 groups) reduces each token once and
+# few tokens (in_rows <= 8 K, at most 1024 groups) reduces each token once and
 # scans row_indices; the rest reduce every destination row.  The cases below
 # reach both: "no_gather" and "tall_short_K" take the per-row kernel.
 @pytest.mark.parametrize("cfg", ["prefill_small", "decode", "negative_ids", "no_gather", "tall_short_K",
