@@ -348,3 +348,23 @@ def test_grouped_nvfp4_extreme_tensor_scales(bsq, kernel):
     p, s = _run_grouped(bsq, "nvfp4", d, 2, kernel=kernel)
     _compare("nvfp4", d, p, s)
 
+
+@pytest.mark.parametrize("G", [1024, 1025])
+def test_grouped_token_kernel_group_limit(bsq, G):
+    """The token kernel keeps the group metadata of up to 1024 groups in
+    shared memory; at 1025 the explicit choice falls back to the band kernel.
+    One- to three-row groups gathered from 900 tokens (rows reused)."""
+    rng = np.random.Generator(np.random.PCG64(G))
+    m = rng.integers(1, 4, size=G)
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = (np.arange(G + 1) * 128).astype(np.uint32)
+    rows = int(ro[-1])
+    x = wl.dense_activations(rng, 900, 128, "blocklognormal")
+    d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=np.arange(G, dtype=np.int32),
+             sf_tensor=np.linspace(0.5, 2.0, G).astype(np.float32),
+             row_indices=rng.integers(0, 900, size=rows).astype(np.int32),
+             total_rows=rows, total_scale_rows=int(so[-1]), G=G)
+    for fmt in ("nvfp4", "mxfp4"):
+        p, s = _run_grouped(bsq, fmt, d, 1, kernel="token")
+        _compare(fmt, d, p, s)
+
