@@ -4,7 +4,7 @@
 // row_offsets[g+1]; its scales go to 5D row scales_offsets[g] + (d -
 // row_offsets[g]) (groups padded to whole 128-row tiles), its NVFP4 tensor
 // scale is sf_tensor[expert_ids[g]], and it reads source row row_indices[d]
-// (or d).  Two kernels, one per regime, give identical bytes:
+// (or d).  Three kernels, one per regime, give identical bytes:
 //
 //  * grouped_band_kernel (groups of many rows, prefill).  A thread block
 //    owns 32 consecutive destination rows, whichever groups they belong to,
@@ -26,6 +26,10 @@
 //    blocks are spread over the lanes, consecutive blocks on consecutive
 //    lanes, each lane quantizing whole blocks; the scale bytes of a row's
 //    atom are OR-reduced over 4 lanes into one word.
+//
+//  * grouped_token_kernel (a row_indices gather that reuses source rows,
+//    top-k routing).  Token-major: each source row is read once and
+//    quantized into all of its destination rows; see its own comment below.
 //
 // Batching column tiles per unit (k_tiles_per_block) amortizes the lookups
 // and makes the grid smaller; at decode, where each unit holds only a few
