@@ -58,3 +58,24 @@ def test_reference_arm_rank_gate(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_contract(monkeypatch, capsys):
+    """Rank 0's reference arm (the oracle on host cores) prints one JSON line
+    with the contract's keys: the arm's own e2e with no host-device bytes, a
+    cpu_baseline describing the run, and the workload named in config."""
+    import json
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["unit"] == "GB/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"]
+
