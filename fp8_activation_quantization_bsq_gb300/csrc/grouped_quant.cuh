@@ -507,7 +507,9 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
 // chunks per step: the block maxima are computed once, and the codes and
 // scale bytes are written for every destination row (MX: the codes are the
 // same for all of them and are encoded once).  A destination row beyond a
-// full bucket is checked and quantized on its own by the warp that found it.
+// full bucket is found again by a re-scan of the block's share after the
+// quantize, then checked and quantized on its own (rare; kept out of the
+// scan loop).
 // Each token row is read from memory once per kTkSlots destination rows,
 // instead of once per destination row.  Needs G <= kTkMaxGroups (group
 // metadata in shared memory).
@@ -526,6 +528,7 @@ struct TkShared {
   uint32_t ro[kTkMaxGroups + 1];
   uint32_t so[kTkMaxGroups + 1];
   int32_t e[kTkMaxGroups];
+  uint32_t overflow;                             // this block's scan found a full bucket
   uint32_t bkt_cnt[kTkClusterTokens];            // this block's scan: rows found per source row
   uint32_t bkt_d[kTkClusterTokens][kTkBucket];   // the first kTkBucket of them
   uint32_t gd[kTkWarps][kTkGather];              // a warp's source row: its gathered rows
@@ -761,8 +764,8 @@ __device__ __forceinline__ uint32_t tk_prepare(const GroupedArgs& a, const uint3
   return div_mask;
 }
 
-// Warp-collective, during the scan: destination rows that lanes found with
-// their bucket full are checked and quantized one at a time by the whole warp.
+// Warp-collective: destination rows that lanes found with their bucket full
+// are checked and quantized one at a time by the whole warp.
 template <int FMT>
 __device__ __forceinline__ void tk_overflow(const GroupedArgs& a, TkShared& sh, bool ov, uint32_t d, int32_t src) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -811,6 +814,7 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
   const bool first_cluster = blockIdx.x < kTkCluster;
   if constexpr (FMT == kNVFP4) fill_div6_table(sh.div6_tab, threadIdx.x, kTkThreads);
   for (int i = threadIdx.x; i < kTkClusterTokens; i += kTkThreads) sh.bkt_cnt[i] = 0u;
+  if (threadIdx.x == 0) sh.overflow = 0u;
   pdl_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0) check_offsets(a);
   for (int i = threadIdx.x; i <= a.G; i += kTkThreads) {
@@ -822,19 +826,21 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
   const int64_t ro_end = sh.ro[a.G];
   const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
 
-  // (1) scan: file the destination rows of the cluster's source rows
+  // the blocks of the cluster split the scan of row_indices: a scalar head
+  // up to a 16-byte boundary and a scalar tail (warp 0 of the first block of
+  // the cluster), and a 16-byte body in kTkCluster contiguous shares
+  const int64_t mis = static_cast<int64_t>(((16 - (reinterpret_cast<uintptr_t>(a.row_indices) & 15)) & 15) >> 2);
+  const int64_t head = mis < rows ? mis : rows;
+  const int64_t nvec = (rows - head) >> 2;
+  const int64_t share = (nvec + kTkCluster - 1) / kTkCluster;
+  const int64_t vb = share * rank;
+  const int64_t ve = vb + share < nvec ? vb + share : nvec;
+
+  // (1) scan: file the destination rows of the cluster's source rows; a row
+  // that finds its bucket full only raises the block's overflow flag (4)
   if (a.row_indices != nullptr) {
-    // the blocks of the cluster split the scan: a scalar head up to a
-    // 16-byte boundary of row_indices and a scalar tail (warp 0 of the first
-    // block), and a 16-byte body in kTkCluster contiguous shares
-    const int64_t mis = static_cast<int64_t>(((16 - (reinterpret_cast<uintptr_t>(a.row_indices) & 15)) & 15) >> 2);
-    const int64_t head = mis < rows ? mis : rows;
-    const int64_t nvec = (rows - head) >> 2;
     const int4* body = reinterpret_cast<const int4*>(a.row_indices + head);
-    const int64_t share = (nvec + kTkCluster - 1) / kTkCluster;
-    const int64_t vb = share * rank;
-    const int64_t ve = vb + share < nvec ? vb + share : nvec;
-    auto file = [&](int64_t d, int32_t src) -> bool {  // true: bucket full
+    auto file = [&](int64_t d, int32_t src) {
       if (src < 0 || src >= a.in_rows) {
         if (first_cluster) {
           uint32_t sr;
@@ -844,24 +850,15 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
         return false;
       }
       const int64_t k = src - c0;
-      if (k < 0 || k >= kTkClusterTokens) return false;
+      if (k < 0 || k >= kTkClusterTokens) return;
       const uint32_t slot = atomicAdd(&sh.bkt_cnt[k], 1u);
-      if (slot < kTkBucket) {
-        sh.bkt_d[k][slot] = static_cast<uint32_t>(d);
-        return false;
-      }
-      return true;
+      if (slot < kTkBucket) sh.bkt_d[k][slot] = static_cast<uint32_t>(d);
+      else sh.overflow = 1u;
     };
     if (rank == 0 && warp == 0) {
       const int64_t d = lane < head ? lane : head + 4 * nvec + (lane - 4);
       const bool in_part = lane < head || (lane >= 4 && lane < 8 && d < rows);
-      int32_t src = 0;
-      bool ov = false;
-      if (in_part) {
-        src = __ldg(a.row_indices + d);
-        ov = file(d, src);
-      }
-      tk_overflow<FMT>(a, sh, ov, static_cast<uint32_t>(d), src);
+      if (in_part) file(d, __ldg(a.row_indices + d));
     }
     constexpr int U = 2;  // 16-byte loads in flight per thread
 #pragma unroll 1
@@ -877,11 +874,8 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
         const int64_t v = v0 + threadIdx.x + u * kTkThreads;
         const int32_t s4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t d = head + 4 * v + j;
-          const bool ov = v < ve && file(d, s4[j]);
-          tk_overflow<FMT>(a, sh, ov, static_cast<uint32_t>(d), s4[j]);
-        }
+        for (int j = 0; j < 4; ++j)
+          if (v < ve) file(head + 4 * v + j, s4[j]);
       }
     }
   }
@@ -949,6 +943,35 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
                                        sh.scale_off[warp], sh.tab[warp])};
       tk_rows<FMT>(a, in_row, va, lst, nb, sh.div6_tab);
       __syncwarp();
+    }
+  }
+  // (4) rows that found their bucket full (rare: more than kTkBucket rows of
+  // one source row in one block's share): the block re-scans its share and
+  // quantizes, one at a time, each row of an overflowed source row that its
+  // bucket does not hold
+  __syncthreads();
+  if (a.row_indices != nullptr && sh.overflow != 0u) {  // block-uniform
+#pragma unroll 1
+    for (int part = 0; part < 3; ++part) {
+      int64_t lo = head + 4 * vb, hi = head + 4 * ve;  // the 16-byte body share
+      if (part == 1) { lo = 0; hi = rank == 0 ? head : 0; }
+      if (part == 2) { lo = head + 4 * nvec; hi = rank == 0 ? rows : lo; }
+#pragma unroll 1
+      for (int64_t d0 = lo; d0 < hi; d0 += kTkThreads) {
+        const int64_t d = d0 + threadIdx.x;
+        int32_t src = 0;
+        bool ov = false;
+        if (d < hi) {
+          src = __ldg(a.row_indices + d);
+          const int64_t k = src - c0;
+          if (src >= 0 && src < a.in_rows && k >= 0 && k < kTkClusterTokens && sh.bkt_cnt[k] > kTkBucket) {
+            ov = true;
+#pragma unroll
+            for (int q = 0; q < kTkBucket; ++q) ov = ov && sh.bkt_d[k][q] != static_cast<uint32_t>(d);
+          }
+        }
+        tk_overflow<FMT>(a, sh, ov, static_cast<uint32_t>(d), src);
+      }
     }
   }
   __syncthreads();
