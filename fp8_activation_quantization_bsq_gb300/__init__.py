@@ -12,6 +12,10 @@ Operations (Modular "block_scaled_quantization" pages):
   quantize            -- quantize_dynamic_block_scaled / quantize_dynamic_scaled_fp4fp8
   grouped_quantize    -- grouped_quantize_dynamic_scaled_fp4_async(_kernel)
   scales_interleave   -- block_scales_interleave(_fp4)(_kernel)
+  block_scaled_dot    -- the idea of naive_block_scaled_matmul (a validator)
+and the steps around them: tensor_sf / grouped_tensor_sf (the NVFP4 tensor
+scales on the GPU), quantize_dynamic (tensor_sf read from device memory),
+gemm_quantize (a matmul with the quantize in its epilogue).
 """
 from __future__ import annotations
 
@@ -221,10 +225,13 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
     [G], ``sf_tensor`` float32 [num_experts] (NVFP4), ``row_indices`` int32 or
     None.  ``total_rows`` / ``total_scale_rows`` size the outputs (required
     when ``out`` / ``scales`` are not given).  ``kernel``: "auto", "stream"
-    (groups of many rows) or "latency" (groups of a few rows); the results
+    (groups of many rows), "latency" (groups of a few rows) or "token" (a
+    row_indices gather that reuses source rows: each read once); the results
     do not depend on it.
     Returns (packed uint8 (total_rows, packed_row_bytes), scales uint8).
     """
+    if kernel not in GROUPED_KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(GROUPED_KERNELS)}")
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
         raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
     f = _fmt(fmt)
