@@ -665,6 +665,18 @@ def run_case(args):
         sys.exit(1)
 
 
+def relaunch_ranks(n: int, argv) -> int:
+    """Start this script as n ranks on this node (one per GPU) through
+    torch.distributed.run on 127.0.0.1 and return its exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -685,7 +697,13 @@ def main(argv=None):
     if args.case is not None:
         run_case(args)
         return
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv)))
     rank, world, local_rank = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match the {world} rank(s) of this launch (WORLD_SIZE)")
+    print(f"bench: rank {rank} of {world} (local rank {local_rank}), impl {args.impl}", file=sys.stderr,
+          flush=True)
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

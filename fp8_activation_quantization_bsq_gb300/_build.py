@@ -43,7 +43,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(LIB_DIR, exist_ok=True)
     tmp = LIB_PATH + ".tmp"
     cmd = [nvcc_path(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo",
-           "-std=c++17", "-shared", "-cudart", "shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+           "-std=c++17", "-Werror", "all-warnings", "-shared", "-cudart", "shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
            "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-I", INCLUDE, "-o", tmp]
     cmd += [os.path.join(CSRC, s) for s in SOURCES]
     res = subprocess.run(cmd, capture_output=True, text=True)

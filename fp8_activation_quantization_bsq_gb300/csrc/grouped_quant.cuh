@@ -847,7 +847,7 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads,
           int e;
           tk_check(a, sh, d, src, sr, e);  // reports the bad source row of a kept group
         }
-        return false;
+        return;
       }
       const int64_t k = src - c0;
       if (k < 0 || k >= kTkClusterTokens) return;

@@ -26,9 +26,13 @@ constexpr int kAmaxMaxBlocks = 1024;
 
 // Dense workspace: a completion counter and one partial per block.  The
 // caller zeroes it once; the last block of every launch sets the counter
-// back to zero, so consecutive launches need no memset in between.  A
-// counter outside [0, gridDim.x) (a workspace never zeroed) records
-// BSQ_ERR_VALUE.
+// back to zero, so consecutive launches need no memset in between.  A stale
+// counter c > 0 (a workspace never zeroed) hands some block a ticket >=
+// gridDim.x, which records BSQ_ERR_VALUE; with c >= gridDim.x no block is
+// last and nothing is written, with a smaller c the block holding ticket
+// gridDim.x - 1 may reduce before the remaining blocks have stored their
+// partials (that launch's outputs are reported as invalid).  Each launch
+// writes every partial it reads, so stale partials are harmless.
 struct AmaxWorkspace {
   unsigned int counter;
   unsigned int pad[3];

@@ -227,9 +227,14 @@ BSQ_API int32_t bsq_quantize_dynamic(int32_t fmt, const void* in_dev, int64_t M,
  *                 device scratch, 16-byte aligned, zeroed by the caller once
  *                 before its first use (e.g. cudaMemsetAsync); every call leaves
  *                 it zeroed again, so consecutive calls need no memset.  A
- *                 workspace that was not zeroed records BSQ_ERR_VALUE in the
- *                 device error word (the outputs are then not written).  Calls
- *                 sharing one workspace must not overlap on the GPU.
+ *                 completion counter that is not zero at launch is reported:
+ *                 BSQ_ERR_VALUE in the device error word.  When the stale
+ *                 counter is at least the launch's block count nothing is
+ *                 written; a smaller stale value can let a block finish the
+ *                 reduction before the others have arrived, so the outputs of
+ *                 a launch that reported BSQ_ERR_VALUE must be discarded.  A
+ *                 workspace left non-zero must be zeroed again before reuse.
+ *                 Calls sharing one workspace must not overlap on the GPU.
  *   The reduction reads in_dev with an L2 evict_last hint, so that a quantize
  *   of the same tensor right after it finds much of it in L2; that quantize
  *   (or any later read with the default policy) returns the lines to normal
@@ -250,10 +255,13 @@ BSQ_API int32_t bsq_tensor_sf(const void* in_dev, int64_t M, int64_t K, int64_t 
  *                 outside [0, in_rows) record BSQ_ERR_VALUE and are skipped.
  *   workspace_dev bsq_grouped_tensor_sf_workspace_bytes(num_experts) bytes of
  *                 device scratch, 16-byte aligned, zeroed by the caller once
- *                 before its first use; every call leaves it zeroed again (as
- *                 for bsq_tensor_sf; a workspace not zeroed records
- *                 BSQ_ERR_VALUE).  Calls sharing one workspace must not overlap
- *                 on the GPU.
+ *                 before its first use; every call leaves it zeroed again.  A
+ *                 stale completion counter is reported as for bsq_tensor_sf
+ *                 (BSQ_ERR_VALUE; discard that launch's outputs).  Stale
+ *                 per-expert maxima under a zero counter are NOT detected:
+ *                 they can only raise an expert's amax, giving a smaller
+ *                 scale, so a workspace must be zeroed whole.  Calls sharing
+ *                 one workspace must not overlap on the GPU.
  */
 BSQ_API int64_t bsq_grouped_tensor_sf_workspace_bytes(int32_t num_experts);
 BSQ_API int32_t bsq_grouped_tensor_sf(const void* in_dev, int64_t in_rows, int64_t K,
@@ -282,6 +290,10 @@ BSQ_API int32_t bsq_grouped_tensor_sf(const void* in_dev, int64_t in_rows, int64
  *   First call    on a device looks up the array's device address and the SM
  *                 count (cudaGetSymbolAddress, cudaDeviceGetAttribute) with that
  *                 device current; make it before any stream capture begins.
+ *                 The address is kept for the life of the process: after a
+ *                 cudaDeviceReset (or any teardown of the device's primary
+ *                 context) it belongs to a context that no longer exists, so
+ *                 do not call this entry point on that device again.
  *   Sharing       every call on a device uses the same array; each call clears
  *                 the part it uses on `stream` first.  Calls that overlap on the
  *                 GPU (other streams, other host threads, without ordering

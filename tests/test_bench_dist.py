@@ -56,7 +56,7 @@ def test_reference_arm_rank_gate(monkeypatch, capsys):
     import bench
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"])
     assert capsys.readouterr().out == ""
 
 
@@ -79,3 +79,30 @@ def test_reference_arm_json_contract(monkeypatch, capsys):
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"]
 
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside torchrun relaunches itself as two ranks;
+    both start (each announces itself on stderr) and rank 0 alone prints the
+    JSON line, with n_gpus 2.  The reference arm needs no GPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, env=env, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert "bench: rank 0 of 2" in res.stderr and "bench: rank 1 of 2" in res.stderr
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_world_size(monkeypatch):
+    """Under a launcher, --gpus must equal WORLD_SIZE: a mismatch is refused
+    (exit status 2) instead of silently running another number of ranks."""
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit) as ei:
+        bench.main(["--impl", "reference", "--gpus", "3", "--steps", "1", "--warmup", "3"])
+    assert ei.value.code == 2

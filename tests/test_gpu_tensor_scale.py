@@ -224,3 +224,29 @@ def test_grouped_dynamic_chain_matches_oracle(bsq, kernel):
     np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
     np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
     assert bsq.device_error() == 0
+
+
+@pytest.mark.parametrize("stale", [1, 0x7FFFFFFF])
+def test_stale_counter_is_reported(bsq, stale):
+    """A completion counter left non-zero is reported (BSQ_ERR_VALUE) for both
+    reductions; with a counter at or past the block count nothing is written
+    (the output keeps its sentinel), with a small stale counter the launch is
+    reported and its output must be discarded."""
+    bits = CASES["large"]()[:2048]
+    x = to_device_bf16(bits)
+    ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    ws[:4].view(torch.int32).fill_(stale)
+    out = torch.full((2,), -7.0, dtype=torch.float32, device="cuda")
+    bsq.tensor_sf(x, out=out, workspace=ws)
+    assert bsq.device_error() == 4
+    if stale >= 1024:
+        np.testing.assert_array_equal(_f32(out), [-7.0, -7.0])
+    d = wl.config_grouped_prefill(seed=5, tokens=200, K=256, num_experts=32, top_k=4)
+    gws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(32), dtype=torch.uint8, device="cuda")
+    gws[:4].view(torch.int32).fill_(stale)
+    gout = torch.full((32,), -7.0, dtype=torch.float32, device="cuda")
+    bsq.grouped_tensor_sf(to_device_bf16(d["x_bits"]), u32_device(d["row_offsets"]), i32_device(d["expert_ids"]),
+                          32, i32_device(d["row_indices"]), total_rows=d["total_rows"], out=gout, workspace=gws)
+    assert bsq.device_error() == 4
+    if stale >= 1024:
+        assert np.all(_f32(gout) == -7.0)
