@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libbsq.so")
 
 SOURCES = ["bsq.cu"]
 HEADERS = ["device_common.cuh", "box_quant.cuh", "dense_quant.cuh", "grouped_quant.cuh", "interleave.cuh",
-           "tensor_scale.cuh", "block_scaled_dot.cuh", "cluster.cuh", "gemm_quant.cuh"]
+           "tensor_scale.cuh", "block_scaled_dot.cuh", "cluster.cuh", "gemm_quant.cuh", "grouped_token.cuh"]
 
 
 def nvcc_path() -> str:

@@ -17,6 +17,7 @@
 #include "gemm_quant.cuh"
 #include "device_common.cuh"
 #include "grouped_quant.cuh"
+#include "grouped_token.cuh"
 #include "interleave.cuh"
 #include "tensor_scale.cuh"
 
@@ -50,6 +51,7 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   int dense_ctas_per_sm[3] = {0, 0, 0};
+  int tq_max_smem = 0;  // dynamic shared memory the token kernel may use
 };
 
 std::mutex g_mu;
@@ -105,6 +107,12 @@ bsq_status device_info(DeviceInfo** out) {
     dense_kernel_setup<kNVFP4>(0, d);
     dense_kernel_setup<kMXFP4>(1, d);
     dense_kernel_setup<kMXFP8>(2, d);
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.tq_max_smem = optin;
+    cudaFuncSetAttribute(grouped_token_kernel<kNVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, d.tq_max_smem);
+    cudaFuncSetAttribute(grouped_token_kernel<kMXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, d.tq_max_smem);
+    cudaFuncSetAttribute(grouped_token_kernel<kMXFP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, d.tq_max_smem);
     if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
     d.ready = true;
   }
@@ -194,16 +202,32 @@ bsq_status launch_grouped_band(GroupedArgs a, cudaStream_t stream) {
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
+// One block per SM, the source rows split evenly; more blocks only when a
+// block would own more than kTqMaxTokens rows.
 template <int FMT>
 bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
-  // source rows the clusters own: with no row_indices every destination row
-  // is its own source row, and rows past in_rows still need their checks
+  DeviceInfo* d = nullptr;
+  if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+  // with no row_indices every destination row is its own source row, and
+  // rows past in_rows still need their checks
   int64_t n_tok = a.row_indices != nullptr ? a.in_rows : std::max(a.in_rows, a.total_rows);
-  n_tok = std::max<int64_t>(n_tok, 1);  // one cluster reports bad source rows
-  const int64_t blocks = ceil_div(n_tok, kTkClusterTokens) * kTkCluster;
+  n_tok = std::max<int64_t>(n_tok, 1);  // block 0 reports bad source rows
+  int64_t blocks = std::min<int64_t>(d->sm_count, n_tok);
+  if (ceil_div(n_tok, blocks) > kTqMaxTokens) blocks = ceil_div(n_tok, kTqMaxTokens);
   if (blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
+  TqArgs q;
+  q.n_tok = n_tok;
+  q.tpb = static_cast<int>(ceil_div(n_tok, blocks));
+  q.n_tab = (FMT == kNVFP4 && a.num_experts <= kTqTabExperts) ? a.num_experts : 0;
+  // row_indices staging: two buffers of up to kTqStageInts entries in what
+  // shared memory is left
+  const size_t fixed = tq_smem_bytes(q.tpb, q.n_tab, 0);
+  if (fixed + 8 * 16 > static_cast<size_t>(d->tq_max_smem)) return BSQ_ERR_SHAPE;
+  const int64_t room = static_cast<int64_t>((static_cast<size_t>(d->tq_max_smem) - fixed) / 8) & ~int64_t(3);
+  q.stage_ints = static_cast<int>(std::min<int64_t>(kTqStageInts, room));
+  const size_t smem = tq_smem_bytes(q.tpb, q.n_tab, q.stage_ints);
   const cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)),
-                                   dim3(kTkThreads), 0, stream, a);
+                                   dim3(kTqThreads), smem, stream, a, q);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -221,16 +245,19 @@ bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t
   if (kernel == BSQ_GROUPED_AUTO) {
     if (a.total_rows <= kGroupedLatencyMaxAvgRows * a.G)
       kernel = BSQ_GROUPED_LATENCY;
-    else if (a.row_indices != nullptr && a.G <= kTkMaxGroups && a.total_rows >= 2 * a.in_rows &&
+    else if (a.row_indices != nullptr && a.G <= kTqMaxGroups && a.total_rows >= 2 * a.in_rows &&
              a.in_rows <= 8 * static_cast<int64_t>(a.K))
-      // source rows reused: read each once.  The clusters' scans read
-      // in_rows * total_rows / 32 bytes of row_indices, in_rows / (64 K) of
-      // the gathered row bytes: kept to at most an eighth.
+      // source rows reused: read each once.  Every block of the token
+      // kernel scans all of row_indices (a few instructions per entry per
+      // SM), which stays small next to the quantize for K >= 256 and
+      // in_rows <= 8 K.
       kernel = BSQ_GROUPED_TOKEN;
     else
       kernel = BSQ_GROUPED_STREAM;
   }
-  if (kernel == BSQ_GROUPED_TOKEN && a.G > kTkMaxGroups) kernel = BSQ_GROUPED_STREAM;
+  // the token kernel files destination rows as 32-bit indices
+  if (kernel == BSQ_GROUPED_TOKEN && (a.G > kTqMaxGroups || a.total_rows >= (int64_t(1) << 32)))
+    kernel = BSQ_GROUPED_STREAM;
   if (kernel == BSQ_GROUPED_TOKEN) return launch_grouped_token<FMT>(a, stream);
   if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_band<FMT>(a, stream);
   switch (kt) {

@@ -27,9 +27,9 @@
 //    lanes, each lane quantizing whole blocks; the scale bytes of a row's
 //    atom are OR-reduced over 4 lanes into one word.
 //
-//  * grouped_token_kernel (a row_indices gather that reuses source rows,
-//    top-k routing).  Token-major: each source row is read once and
-//    quantized into all of its destination rows; see its own comment below.
+//  * grouped_token_kernel (grouped_token.cuh; a row_indices gather that
+//    reuses source rows, top-k routing).  Token-major: each source row is
+//    read once and quantized into all of its destination rows.
 //
 // Batching column tiles per unit (k_tiles_per_block) amortizes the lookups
 // and makes the grid smaller; at decode, where each unit holds only a few
@@ -38,7 +38,6 @@
 #pragma once
 
 #include "box_quant.cuh"
-#include "cluster.cuh"
 #include "device_common.cuh"
 
 namespace bsq {
@@ -493,114 +492,7 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
   }
 }
 
-// ----------------------------------------------------- grouped_token_kernel --
-//
-// Token-major, for gathers that reuse source rows (top-k routing: each token
-// row feeds k destination rows).  A cluster of kTkCluster blocks owns
-// kTkClusterTokens consecutive source rows, one per warp.  (1) The cluster's
-// blocks split one scan of row_indices; each block files the destination
-// rows whose source row the cluster owns into per-source-row buckets in its
-// own shared memory.  (2) Each warp gathers its source row's destination
-// rows from the buckets of all blocks of the cluster (distributed shared
-// memory), checks them as the other kernels do, and (3) reads its source row
-// once per kTkSlots destination rows, 32 lanes on 32 consecutive 32-element
-// chunks per step: the block maxima are computed once, and the codes and
-// scale bytes are written for every destination row (MX: the codes are the
-// same for all of them and are encoded once).  A destination row beyond a
-// full bucket is found again by a re-scan of the block's share after the
-// quantize, then checked and quantized on its own (rare; kept out of the
-// scan loop).
-// Each token row is read from memory once per kTkSlots destination rows,
-// instead of once per destination row.  Needs G <= kTkMaxGroups (group
-// metadata in shared memory).
-
-constexpr int kTkWarps = 16;
-constexpr int kTkThreads = 32 * kTkWarps;
-constexpr int kTkTokens = kTkWarps;  // source rows per block, one per warp
-constexpr int kTkCluster = 8;
-constexpr int kTkClusterTokens = kTkCluster * kTkTokens;
-constexpr int kTkBucket = 8;         // destination rows one block's scan files per source row
-constexpr int kTkGather = kTkCluster * kTkBucket;
-constexpr int kTkSlots = 16;         // destination rows per pass over a source row
-constexpr int kTkMaxGroups = 1024;
-
-struct TkShared {
-  uint32_t ro[kTkMaxGroups + 1];
-  uint32_t so[kTkMaxGroups + 1];
-  int32_t e[kTkMaxGroups];
-  uint32_t overflow;                             // this block's scan found a full bucket
-  uint32_t bkt_cnt[kTkClusterTokens];            // this block's scan: rows found per source row
-  uint32_t bkt_d[kTkClusterTokens][kTkBucket];   // the first kTkBucket of them
-  uint32_t gd[kTkWarps][kTkGather];              // a warp's source row: its gathered rows
-  uint32_t dst[kTkWarps][kTkSlots];              // a pass: destination rows,
-  uint32_t srow[kTkWarps][kTkSlots];             // their 5D scale rows,
-  float tsf[kTkWarps][kTkSlots];                 // tensor scales,
-  int64_t out_off[kTkWarps][kTkSlots];           // output offsets,
-  int64_t scale_off[kTkWarps][kTkSlots];         // 5D scale offsets,
-  float tab[kTkWarps][kTkSlots][16];             // NVFP4 factor tables
-  float div6_tab[128];
-};
-
-// Destination row d (< min(row_offsets[G], total_rows)) reading source row
-// src: the checks of the other kernels.  Returns true, with its 5D scale row
-// and expert, when d is to be quantized; records BSQ_ERR_VALUE for
-// inconsistent metadata and for a source row outside x in a kept group.
-__device__ __forceinline__ bool tk_check(const GroupedArgs& a, const TkShared& sh, int64_t d, int64_t src,
-                                         uint32_t& srow_out, int& e_out) {
-  int lo = 0, hi = a.G - 1;  // g = max{g : ro[g] <= d}
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (static_cast<int64_t>(sh.ro[mid + 1]) <= d) lo = mid + 1;
-    else hi = mid;
-  }
-  const int64_t r_beg = sh.ro[lo], r_end = sh.ro[lo + 1], so_g = sh.so[lo], so_n = sh.so[lo + 1];
-  const int e = sh.e[lo];
-  const int64_t srow = so_g + (d - r_beg);
-  if (r_end - r_beg < 0 || r_end - r_beg > so_n - so_g || r_end > a.total_rows ||
-      srow >= a.total_scale_rows || d < r_beg || d >= r_end || (a.sf != nullptr && e >= a.num_experts)) {
-    record_error(kErrValue);
-    return false;
-  }
-  if (e < 0) return false;
-  if (src < 0 || src >= a.in_rows) {
-    record_error(kErrValue);
-    return false;
-  }
-  srow_out = static_cast<uint32_t>(srow);  // < scales_offsets[g + 1], a uint32
-  e_out = e;
-  return true;
-}
-
-// quant8_e2m1 with the BF16 -> FP32 widening done by fma.rn.f32.bf16(x, 1, -0)
-// (exact, sign of zero kept) on the FMA pipe instead of shifts and masks on
-// the integer pipe, which the token kernel's per-destination loop keeps busy.
-__device__ __forceinline__ uint32_t quant8_e2m1_fw(uint4 w, float f) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, one;\n\t"
-      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
-      ".reg .b64 p0, p1, p2, p3, ff;\n\t"
-      ".reg .b8 q0, q1, q2, q3;\n\t"
-      "mov.b16 one, 0x3F80;\n\t"
-      "mov.b32 {x0, x1}, %1;\n\tmov.b32 {x2, x3}, %2;\n\t"
-      "mov.b32 {x4, x5}, %3;\n\tmov.b32 {x6, x7}, %4;\n\t"
-      "fma.rn.f32.bf16 y0, x0, one, 0f80000000;\n\tfma.rn.f32.bf16 y1, x1, one, 0f80000000;\n\t"
-      "fma.rn.f32.bf16 y2, x2, one, 0f80000000;\n\tfma.rn.f32.bf16 y3, x3, one, 0f80000000;\n\t"
-      "fma.rn.f32.bf16 y4, x4, one, 0f80000000;\n\tfma.rn.f32.bf16 y5, x5, one, 0f80000000;\n\t"
-      "fma.rn.f32.bf16 y6, x6, one, 0f80000000;\n\tfma.rn.f32.bf16 y7, x7, one, 0f80000000;\n\t"
-      "mov.b64 ff, {%5, %5};\n\t"
-      "mov.b64 p0, {y0, y1};\n\tmul.rn.f32x2 p0, p0, ff;\n\tmov.b64 {y0, y1}, p0;\n\t"
-      "mov.b64 p1, {y2, y3};\n\tmul.rn.f32x2 p1, p1, ff;\n\tmov.b64 {y2, y3}, p1;\n\t"
-      "mov.b64 p2, {y4, y5};\n\tmul.rn.f32x2 p2, p2, ff;\n\tmov.b64 {y4, y5}, p2;\n\t"
-      "mov.b64 p3, {y6, y7};\n\tmul.rn.f32x2 p3, p3, ff;\n\tmov.b64 {y6, y7}, p3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q0, y1, y0;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q1, y3, y2;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q2, y5, y4;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q3, y7, y6;\n\t"
-      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
-      : "=r"(r)
-      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "f"(f));
-  return r;
-}
+// ------------------------------------------------------ NVFP4 factor table --
 
 // NVFP4 element scale tsf / ds for one destination row without a division.
 // A positive E4M3 scale byte b decodes to ds = m * 2^-(shift) with m a small
@@ -618,364 +510,6 @@ __device__ __forceinline__ float tk_factor(const float* tab, uint32_t b) {
   const uint32_t m = (b & 7u) | (E != 0u ? 8u : 0u);
   const uint32_t e_eff = E != 0u ? E : 1u;
   return __fmul_rn(tab[m], __uint_as_float((137u - e_eff) << 23));  // * 2^(10 - e_eff)
-}
-
-// Warp w quantizes source row in_row into the n destination rows of list
-// `l` (TkList: output byte offsets, 5D scale-row offsets, tensor scales and,
-// for NVFP4, factor tables).  va holds the first step's chunk (lane's chunk
-// `lane`), loaded by the caller.
-struct TkList {
-  const int64_t* out_off;   // destination row * packed row bytes
-  const int64_t* scale_off; // 5D offset of the row's word in its first atom
-  const float* tsf;
-  const float (*tab)[16];   // NVFP4: tsf / m tables (nullptr: divide)
-  uint32_t div_mask;        // NVFP4: rows whose tsf is outside the table range
-};
-
-template <int FMT>
-__device__ __forceinline__ void tk_rows(const GroupedArgs& a, const uint16_t* in_row, uint4 (&va)[4],
-                                        const TkList& l, int n, const float* div6_tab) {
-  constexpr int SF = Fmt<FMT>::SF;
-  constexpr int CPA = 4 / (32 / SF);  // chunks per 5D atom
-  const int lane = threadIdx.x & 31;
-  const int n_chunks = a.K / 32;
-  const int c_pad = a.kt_atoms * CPA;
-  const bool in_vec32 = a.in_vec32 != 0, out_vec32 = a.out_vec32 != 0;
-  int ch = lane;
-  uint4 vb[4]{};  // MX: a second step in flight
-  if constexpr (FMT != kNVFP4) {
-    if (ch + 32 < n_chunks) band_load(vb, in_row + 32 * (ch + 32), in_vec32);
-  }
-#pragma unroll 1
-  for (int c0 = 0; c0 < c_pad; c0 += 32, ch += 32) {
-    uint4 v[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = va[c];
-    if constexpr (FMT == kNVFP4) {
-      if (ch + 32 < n_chunks) band_load(va, in_row + 32 * (ch + 32), in_vec32);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) va[c] = vb[c];
-      if (ch + 64 < n_chunks) band_load(vb, in_row + 32 * (ch + 64), in_vec32);
-    }
-    const bool has = ch < n_chunks;
-    if (!has) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    const bool store_word = (lane % CPA) == 0 && ch < c_pad;
-    const int64_t atom = static_cast<int64_t>(ch / CPA) * 512;
-    const int64_t elem = static_cast<int64_t>(ch) * (Fmt<FMT>::OUT_BITS == 4 ? 16 : 32);
-    if constexpr (FMT == kNVFP4) {
-      float a6[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int c = 2 * j; c < 2 * j + 2; ++c) {
-          acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
-          acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
-        }
-        a6[j] = amax_div6(absmax_final(acc), div6_tab);
-      }
-#pragma unroll 1
-      for (int i = 0; i < n; ++i) {
-        const float tsf = l.tsf[i];
-        const uint32_t b0 = f32_to_e4m3(__fmul_rn(a6[0], tsf)), b1 = f32_to_e4m3(__fmul_rn(a6[1], tsf));
-        float f0, f1;
-        if ((l.div_mask >> i) & 1u) {  // warp-uniform
-          const float d0 = e4m3_to_f32(b0), d1 = e4m3_to_f32(b1);
-          f0 = d0 == 0.0f ? 0.0f : __fdiv_rn(tsf, d0);
-          f1 = d1 == 0.0f ? 0.0f : __fdiv_rn(tsf, d1);
-        } else {
-          f0 = tk_factor(l.tab[i], b0);
-          f1 = tk_factor(l.tab[i], b1);
-        }
-        if (has)
-          st_global_v4(a.out + l.out_off[i] + elem, quant8_e2m1_fw(v[0], f0), quant8_e2m1_fw(v[1], f0),
-                       quant8_e2m1_fw(v[2], f1), quant8_e2m1_fw(v[3], f1));
-        uint32_t word = has ? (b0 | b1 << 8) << (16 * (lane & 1)) : 0u;
-        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-        if (store_word) *reinterpret_cast<uint32_t*>(a.scales + l.scale_off[i] + atom) = word;
-      }
-    } else {
-      uint32_t acc = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc = absmax2(acc, v[c].x); acc = absmax2(acc, v[c].y);
-        acc = absmax2(acc, v[c].z); acc = absmax2(acc, v[c].w);
-      }
-      const MxScale sc = mx_scale<FMT == kMXFP4 ? 6 : 448>(absmax_final(acc));
-      uint32_t word = has ? sc.byte << (8 * (lane & 3)) : 0u;
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-      uint32_t o[8];
-      if constexpr (FMT == kMXFP4) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[c] = quant8_e2m1_pow2(v[c], sc.pow2);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint2 q = quant8_e4m3_pow2(v[c], sc.pow2);
-          o[2 * c] = q.x;
-          o[2 * c + 1] = q.y;
-        }
-      }
-#pragma unroll 1
-      for (int i = 0; i < n; ++i) {
-        uint8_t* dst = a.out + l.out_off[i] + elem;
-        if (has) {
-          if constexpr (FMT == kMXFP4) {
-            st_global_v4(dst, o[0], o[1], o[2], o[3]);
-          } else if (out_vec32) {
-            st_global_v8(dst, o);
-          } else {
-            st_global_v4(dst, o[0], o[1], o[2], o[3]);
-            st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
-          }
-        }
-        if (store_word) *reinterpret_cast<uint32_t*>(a.scales + l.scale_off[i] + atom) = word;
-      }
-    }
-  }
-}
-
-// The per-row offsets of a list of destination rows (and, NVFP4, the factor
-// tables), lanes over rows: entries [0, n) of the arrays.
-template <int FMT>
-__device__ __forceinline__ uint32_t tk_prepare(const GroupedArgs& a, const uint32_t* dsts, const uint32_t* srows,
-                                               const float* tsfs, int n, int64_t* out_off, int64_t* scale_off,
-                                               float (*tab)[16]) {
-  const int lane = threadIdx.x & 31;
-  if (lane < n) {
-    const int64_t sr = srows[lane];
-    out_off[lane] = static_cast<int64_t>(dsts[lane]) * a.out_ld;
-    scale_off[lane] = (sr >> 7) * static_cast<int64_t>(a.kt_atoms) * 512 + (sr & 31) * 16 + ((sr & 127) >> 5) * 4;
-  }
-  uint32_t div_mask = 0u;
-  if constexpr (FMT == kNVFP4) {
-    div_mask = __ballot_sync(0xFFFFFFFFu, lane < n && !tk_factor_table_ok(tsfs[lane < n ? lane : 0]));
-    for (int idx = lane; idx < 16 * n; idx += 32) {
-      const int i = idx >> 4, m = idx & 15;
-      tab[i][m] = m == 0 ? 0.0f : __fdiv_rn(tsfs[i], static_cast<float>(m));
-    }
-  }
-  __syncwarp();
-  return div_mask;
-}
-
-// Warp-collective: destination rows that lanes found with their bucket full
-// are checked and quantized one at a time by the whole warp.
-template <int FMT>
-__device__ __forceinline__ void tk_overflow(const GroupedArgs& a, TkShared& sh, bool ov, uint32_t d, int32_t src) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t m = __ballot_sync(0xFFFFFFFFu, ov);
-  while (m != 0u) {
-    const int l = __ffs(m) - 1;
-    m &= m - 1u;
-    const uint32_t dd = __shfl_sync(0xFFFFFFFFu, d, l);
-    const int32_t ss = __shfl_sync(0xFFFFFFFFu, src, l);
-    int ok = 0;
-    if (lane == 0) {
-      uint32_t sr = 0;
-      int e = -1;
-      ok = tk_check(a, sh, dd, ss, sr, e);
-      if (ok) {
-        sh.dst[warp][0] = dd;
-        sh.srow[warp][0] = sr;
-        sh.tsf[warp][0] = a.sf != nullptr ? __ldg(a.sf + e) : 1.0f;
-      }
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    __syncwarp();
-    if (ok) {  // warp-uniform
-      const uint16_t* in_row = a.in + static_cast<int64_t>(ss) * a.ld_in;
-      uint4 va[4]{};
-      if (lane < a.K / 32) band_load(va, in_row + 32 * lane, a.in_vec32 != 0);
-      const TkList lst{sh.out_off[warp], sh.scale_off[warp], sh.tsf[warp], sh.tab[warp],
-                       tk_prepare<FMT>(a, sh.dst[warp], sh.srow[warp], sh.tsf[warp], 1, sh.out_off[warp],
-                                       sh.scale_off[warp], sh.tab[warp])};
-      tk_rows<FMT>(a, in_row, va, lst, 1, sh.div6_tab);
-      __syncwarp();
-    }
-  }
-}
-
-// Grid: a multiple of kTkCluster blocks covering the source rows (with no
-// row_indices: max(in_rows, total_rows), destination row d reading row d).
-template <int FMT>
-__global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTkThreads, 2)
-    grouped_token_kernel(const GroupedArgs a) {
-  __shared__ TkShared sh;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = static_cast<int>(blockIdx.x % kTkCluster);
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x / kTkCluster) * kTkClusterTokens;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTkTokens;
-  const bool first_cluster = blockIdx.x < kTkCluster;
-  if constexpr (FMT == kNVFP4) fill_div6_table(sh.div6_tab, threadIdx.x, kTkThreads);
-  for (int i = threadIdx.x; i < kTkClusterTokens; i += kTkThreads) sh.bkt_cnt[i] = 0u;
-  if (threadIdx.x == 0) sh.overflow = 0u;
-  pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0) check_offsets(a);
-  for (int i = threadIdx.x; i <= a.G; i += kTkThreads) {
-    sh.ro[i] = __ldg(a.row_offsets + i);
-    sh.so[i] = __ldg(a.scales_offsets + i);
-    if (i < a.G) sh.e[i] = __ldg(a.expert_ids + i);
-  }
-  __syncthreads();
-  const int64_t ro_end = sh.ro[a.G];
-  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
-
-  // the blocks of the cluster split the scan of row_indices: a scalar head
-  // up to a 16-byte boundary and a scalar tail (warp 0 of the first block of
-  // the cluster), and a 16-byte body in kTkCluster contiguous shares
-  const int64_t mis = static_cast<int64_t>(((16 - (reinterpret_cast<uintptr_t>(a.row_indices) & 15)) & 15) >> 2);
-  const int64_t head = mis < rows ? mis : rows;
-  const int64_t nvec = (rows - head) >> 2;
-  const int64_t share = (nvec + kTkCluster - 1) / kTkCluster;
-  const int64_t vb = share * rank;
-  const int64_t ve = vb + share < nvec ? vb + share : nvec;
-
-  // (1) scan: file the destination rows of the cluster's source rows; a row
-  // that finds its bucket full only raises the block's overflow flag (4)
-  if (a.row_indices != nullptr) {
-    const int4* body = reinterpret_cast<const int4*>(a.row_indices + head);
-    auto file = [&](int64_t d, int32_t src) {
-      if (src < 0 || src >= a.in_rows) {
-        if (first_cluster) {
-          uint32_t sr;
-          int e;
-          tk_check(a, sh, d, src, sr, e);  // reports the bad source row of a kept group
-        }
-        return;
-      }
-      const int64_t k = src - c0;
-      if (k < 0 || k >= kTkClusterTokens) return;
-      const uint32_t slot = atomicAdd(&sh.bkt_cnt[k], 1u);
-      if (slot < kTkBucket) sh.bkt_d[k][slot] = static_cast<uint32_t>(d);
-      else sh.overflow = 1u;
-    };
-    if (rank == 0 && warp == 0) {
-      const int64_t d = lane < head ? lane : head + 4 * nvec + (lane - 4);
-      const bool in_part = lane < head || (lane >= 4 && lane < 8 && d < rows);
-      if (in_part) file(d, __ldg(a.row_indices + d));
-    }
-    constexpr int U = 2;  // 16-byte loads in flight per thread
-#pragma unroll 1
-    for (int64_t v0 = vb; v0 < ve; v0 += static_cast<int64_t>(kTkThreads) * U) {
-      int4 q[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t v = v0 + threadIdx.x + u * kTkThreads;
-        q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t v = v0 + threadIdx.x + u * kTkThreads;
-        const int32_t s4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (v < ve) file(head + 4 * v + j, s4[j]);
-      }
-    }
-  }
-  __syncthreads();
-  cluster_sync_all();  // every block's buckets are complete
-
-  // (2) gather this warp's source row's destination rows
-  const int64_t t = t0 + warp;
-  uint32_t nd = 0;
-  if (a.row_indices != nullptr) {
-    const int k = rank * kTkTokens + warp;
-    uint32_t c = 0;
-    if (lane < kTkCluster) c = min(cluster_ld_u32(cluster_map(&sh.bkt_cnt[k], lane)), static_cast<uint32_t>(kTkBucket));
-    uint32_t incl = c;
-#pragma unroll
-    for (int off = 1; off < kTkCluster; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    const uint32_t excl = incl - c;
-    nd = __shfl_sync(0xFFFFFFFFu, incl, kTkCluster - 1);
-    uint32_t ex[kTkCluster];
-#pragma unroll
-    for (int q = 0; q < kTkCluster; ++q) ex[q] = __shfl_sync(0xFFFFFFFFu, excl, q);
-    for (uint32_t j = lane; j < nd; j += 32) {
-      int r = 0;  // the last block whose run starts at or before j holds entry j
-      uint32_t run = 0;
-#pragma unroll
-      for (int q = 1; q < kTkCluster; ++q) {
-        if (ex[q] <= j) {
-          r = q;
-          run = ex[q];
-        }
-      }
-      sh.gd[warp][j] = cluster_ld_u32(cluster_map(&sh.bkt_d[k][j - run], r));
-    }
-  } else if (t < rows) {
-    if (lane == 0) sh.gd[warp][0] = static_cast<uint32_t>(t);  // destination row t reads row t
-    nd = 1;
-  }
-  __syncwarp();
-
-  // (3) check the rows and quantize them, kTkSlots per pass over the source row
-  for (uint32_t base = 0; base < nd; base += 32) {
-    const uint32_t j = base + lane;
-    uint32_t d = 0, sr = 0;
-    int e = -1;
-    const bool ok = j < nd && tk_check(a, sh, d = sh.gd[warp][j], t, sr, e);
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
-    const int pos = __popc(m & ((1u << lane) - 1u)), cnt = __popc(m);
-    const float tsf = ok && a.sf != nullptr ? __ldg(a.sf + e) : 1.0f;
-    for (int p0 = 0; p0 < cnt; p0 += kTkSlots) {
-      if (ok && pos >= p0 && pos < p0 + kTkSlots) {
-        sh.dst[warp][pos - p0] = d;
-        sh.srow[warp][pos - p0] = sr;
-        sh.tsf[warp][pos - p0] = tsf;
-      }
-      __syncwarp();
-      const int nb = min(cnt - p0, kTkSlots);
-      const uint16_t* in_row = a.in + t * a.ld_in;
-      uint4 va[4]{};
-      if (lane < a.K / 32) band_load(va, in_row + 32 * lane, a.in_vec32 != 0);
-      const TkList lst{sh.out_off[warp], sh.scale_off[warp], sh.tsf[warp], sh.tab[warp],
-                       tk_prepare<FMT>(a, sh.dst[warp], sh.srow[warp], sh.tsf[warp], nb, sh.out_off[warp],
-                                       sh.scale_off[warp], sh.tab[warp])};
-      tk_rows<FMT>(a, in_row, va, lst, nb, sh.div6_tab);
-      __syncwarp();
-    }
-  }
-  // (4) rows that found their bucket full (rare: more than kTkBucket rows of
-  // one source row in one block's share): the block re-scans its share and
-  // quantizes, one at a time, each row of an overflowed source row that its
-  // bucket does not hold
-  __syncthreads();
-  if (a.row_indices != nullptr && sh.overflow != 0u) {  // block-uniform
-#pragma unroll 1
-    for (int part = 0; part < 3; ++part) {
-      int64_t lo = head + 4 * vb, hi = head + 4 * ve;  // the 16-byte body share
-      if (part == 1) { lo = 0; hi = rank == 0 ? head : 0; }
-      if (part == 2) { lo = head + 4 * nvec; hi = rank == 0 ? rows : lo; }
-#pragma unroll 1
-      for (int64_t d0 = lo; d0 < hi; d0 += kTkThreads) {
-        const int64_t d = d0 + threadIdx.x;
-        int32_t src = 0;
-        bool ov = false;
-        if (d < hi) {
-          src = __ldg(a.row_indices + d);
-          const int64_t k = src - c0;
-          if (src >= 0 && src < a.in_rows && k >= 0 && k < kTkClusterTokens && sh.bkt_cnt[k] > kTkBucket) {
-            ov = true;
-#pragma unroll
-            for (int q = 0; q < kTkBucket; ++q) ov = ov && sh.bkt_d[k][q] != static_cast<uint32_t>(d);
-          }
-        }
-        tk_overflow<FMT>(a, sh, ov, static_cast<uint32_t>(d), src);
-      }
-    }
-  }
-  __syncthreads();
-  cluster_sync_all();  // no block leaves while another may still read its buckets
 }
 
 }  // namespace bsq

@@ -1,0 +1,482 @@
+// Token-major grouped quantize for row_indices gathers that reuse source rows
+// (top-k MoE routing: every token row feeds k destination rows).
+//
+// Persistent: one 1024-thread block per SM, each owning an equal share of
+// the source rows (tokens), so every SM gets the same work when tokens carry
+// the same number of destination rows.  A block
+//   (1) issues each warp's first token-row loads, then scans all of
+//       row_indices itself (16-byte loads; the 128 KB of a 32768-row prefill
+//       stay in L2 for the other blocks) and files every destination row
+//       whose source row it owns into a per-token bucket in shared memory;
+//   (2) builds, per token, the list of its destination rows (group, 5D scale
+//       row, expert scale: the same checks as the other grouped kernels);
+//   (3) streams the token row once, 32 lanes on 32 consecutive scale blocks
+//       per step, computing each block's maximum and widening its elements
+//       to FP32 once, then for every destination row only the per-row scale,
+//       the products and the conversions (MX: the codes do not depend on the
+//       row and are encoded once, then stored per row).
+// A token with more destination rows than a bucket holds is left to a
+// re-scan after the others (rare: never with top-k routing to distinct
+// experts); its rows are then quantized one at a time.
+//
+// NVFP4 element scale tsf / ds without a division: per expert a table of
+// fl32(tsf / m), m = 1..15, and tk_factor's power-of-two step (exact for
+// 2^-117 <= tsf <= 2^118; other scales divide).
+#pragma once
+
+#include "grouped_quant.cuh"
+
+namespace bsq {
+
+constexpr int kTqWarps = 32;
+constexpr int kTqThreads = 32 * kTqWarps;
+constexpr int kTqBucket = 16;        // destination rows kept per token (more: the re-scan path)
+constexpr int kTqMaxTokens = 512;    // tokens per block at most (more: more blocks)
+constexpr int kTqMaxGroups = 1024;   // group metadata held in shared memory
+constexpr int kTqTabExperts = 1024;  // NVFP4: experts with a factor table in shared memory
+constexpr int kTqStageInts = 16384;  // row_indices entries per staging buffer at most (64 KB)
+
+// One destination row of the token a warp is quantizing.
+struct alignas(16) TqDesc {
+  uint8_t* out;    // its packed row
+  uint8_t* scale;  // its byte in the first 5D atom of its scale row
+  float tsf;       // NVFP4 tensor scale of its expert
+  int tab;         // NVFP4: offset of the expert's factor table (floats), -1: divide
+};
+
+struct TqShared {
+  uint32_t ro[kTqMaxGroups + 1];
+  uint32_t so[kTqMaxGroups + 1];
+  int32_t e[kTqMaxGroups];
+  TqDesc desc[kTqWarps][kTqBucket];
+  float div6_tab[128];
+  uint64_t stage_bar[2];  // completion of the two row_indices staging buffers
+  uint32_t heavy;         // some token of this block has more rows than its bucket
+  uint32_t failed;        // a staging wait expired
+};
+
+// Launch constants of the token kernel (host-computed).
+struct TqArgs {
+  int64_t n_tok;  // source rows split over the blocks
+  int tpb;        // tokens per block at most (size of the buckets)
+  int n_tab;      // NVFP4 experts with a factor table (0: every row divides)
+  int stage_ints; // row_indices entries per staging buffer (a multiple of 4)
+};
+
+// Dynamic shared memory: TqShared, two row_indices staging buffers, the
+// buckets (tpb counts and tpb x kTqBucket rows) and the NVFP4 tables.
+__host__ __device__ constexpr size_t tq_smem_bytes(int tpb, int n_tab, int stage_ints) {
+  return sizeof(TqShared) + static_cast<size_t>(stage_ints) * 8 + static_cast<size_t>(tpb) * (kTqBucket + 1) * 4 +
+         static_cast<size_t>(n_tab) * 64;
+}
+
+// 1D bulk copy (TMA) of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Destination row d (< min(row_offsets[G], total_rows)) reading source row
+// src: the checks of the other kernels, on group metadata in shared memory.
+// True (with the 5D scale row and the expert) when d is to be quantized;
+// BSQ_ERR_VALUE for inconsistent metadata and for a source row outside x in
+// a kept group.
+__device__ __forceinline__ bool tq_check(const GroupedArgs& a, const TqShared& sh, int64_t d, int64_t src,
+                                         int64_t& srow_out, int& e_out) {
+  int lo = 0, hi = a.G - 1;  // g = max{g : ro[g] <= d}
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(sh.ro[mid + 1]) <= d) lo = mid + 1;
+    else hi = mid;
+  }
+  const int64_t r_beg = sh.ro[lo], r_end = sh.ro[lo + 1], so_g = sh.so[lo], so_n = sh.so[lo + 1];
+  const int e = sh.e[lo];
+  const int64_t srow = so_g + (d - r_beg);
+  if (r_end - r_beg < 0 || r_end - r_beg > so_n - so_g || r_end > a.total_rows ||
+      srow >= a.total_scale_rows || d < r_beg || d >= r_end || (a.sf != nullptr && e >= a.num_experts)) {
+    record_error(kErrValue);
+    return false;
+  }
+  if (e < 0) return false;
+  if (src < 0 || src >= a.in_rows) {
+    record_error(kErrValue);
+    return false;
+  }
+  srow_out = srow;
+  e_out = e;
+  return true;
+}
+
+// Lanes [0, n) hold candidate destination rows d of source row t; the valid
+// ones become the warp's descriptors 0..(count-1).  Returns the count.
+template <int FMT>
+__device__ __forceinline__ int tq_describe(const GroupedArgs& a, TqShared& sh, TqDesc* desc, bool cand,
+                                           int64_t d, int64_t t, int n_tab) {
+  const int lane = threadIdx.x & 31;
+  int64_t srow = 0;
+  int e = 0;
+  const bool ok = cand && tq_check(a, sh, d, t, srow, e);
+  const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
+  if (ok) {
+    TqDesc dd;
+    dd.out = a.out + d * a.out_ld;
+    dd.scale = a.scales + (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512 + (srow & 31) * 16 +
+               ((srow & 127) >> 5) * 4;
+    dd.tsf = 1.0f;
+    dd.tab = -1;
+    if constexpr (FMT == kNVFP4) {
+      dd.tsf = __ldg(a.sf + e);
+      if (e < n_tab && tk_factor_table_ok(dd.tsf)) dd.tab = e * 16;
+    }
+    desc[__popc(m & ((1u << lane) - 1u))] = dd;
+  }
+  __syncwarp();
+  return __popc(m);
+}
+
+// A lane's step data: one NVFP4 block (16 elements) or one MX block (32).
+template <int FMT> struct TqChunk { uint4 v[Fmt<FMT>::SF / 8]; };
+
+template <int FMT>
+__device__ __forceinline__ void tq_load(TqChunk<FMT>& c, const uint16_t* p, bool vec32) {
+#pragma unroll
+  for (int i = 0; i < Fmt<FMT>::SF / 8; i += 2) {
+    if (vec32) {
+      ld_global_nc_v8(p + 8 * i, c.v[i], c.v[i + 1]);
+    } else {
+      c.v[i] = ld_global_nc_v4(p + 8 * i);
+      c.v[i + 1] = ld_global_nc_v4(p + 8 * (i + 1));
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void tq_zero(TqChunk<FMT>& c) {
+#pragma unroll
+  for (int i = 0; i < Fmt<FMT>::SF / 8; ++i) c.v[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// 8 FP32 values (four pairs, element 0 first) -> 8 E2M1 codes in one word.
+__device__ __forceinline__ uint32_t e2m1_word(float2 p0, float2 p1, float2 p2, float2 p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(r)
+      : "f"(p0.x), "f"(p0.y), "f"(p1.x), "f"(p1.y), "f"(p2.x), "f"(p2.y), "f"(p3.x), "f"(p3.y));
+  return r;
+}
+
+__device__ __forceinline__ void st_global_u8(void* p, uint32_t v) {
+  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// The warp quantizes the scale blocks [jb, je) of source row in_row (jb a
+// multiple of 32, je <= the row's blocks with a scale byte) into its nv
+// described destination rows, 32 blocks per step, lane l on block jb + l,
+// jb + 32 + l, ...  cur holds the lane's block of the first step.
+template <int FMT>
+__device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_row, TqChunk<FMT>& cur, int jb,
+                                       int je, const TqDesc* desc, int nv, const float* div6_tab,
+                                       const float* tabs) {
+  constexpr int SF = Fmt<FMT>::SF;
+  const int lane = threadIdx.x & 31;
+  const int S = a.K / SF;          // blocks with data
+  const int S4 = a.kt_atoms * 4;   // blocks with a scale byte (the last atom's padding is 0x00)
+  const bool vec32 = a.in_vec32 != 0;
+#pragma unroll 1
+  for (int j = jb + lane; j - lane < je; j += 32) {
+    TqChunk<FMT> nx;
+    tq_zero(nx);
+    if (j - lane + 32 < je && j + 32 < S) tq_load(nx, in_row + SF * (j + 32), vec32);
+    const bool has = j < S, has_scale = j < S4;
+    const int64_t sc_off = static_cast<int64_t>(j >> 2) * 512 + (j & 3);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int c = 0; c < SF / 8; ++c) {
+      acc = absmax2(acc, cur.v[c].x); acc = absmax2(acc, cur.v[c].y);
+      acc = absmax2(acc, cur.v[c].z); acc = absmax2(acc, cur.v[c].w);
+    }
+    const float amax = absmax_final(acc);
+    if constexpr (FMT == kNVFP4) {
+      const float a6 = amax_div6(amax, div6_tab);
+      float2 y[8];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        y[4 * c + 0] = make_float2(bf16_lo(cur.v[c].x), bf16_hi(cur.v[c].x));
+        y[4 * c + 1] = make_float2(bf16_lo(cur.v[c].y), bf16_hi(cur.v[c].y));
+        y[4 * c + 2] = make_float2(bf16_lo(cur.v[c].z), bf16_hi(cur.v[c].z));
+        y[4 * c + 3] = make_float2(bf16_lo(cur.v[c].w), bf16_hi(cur.v[c].w));
+      }
+      const int64_t el_off = static_cast<int64_t>(j) * 8;
+#pragma unroll 1
+      for (int i = 0; i < nv; ++i) {
+        const TqDesc dd = desc[i];
+        const uint32_t b = f32_to_e4m3(__fmul_rn(a6, dd.tsf));
+        float f;
+        if (dd.tab < 0) {  // warp-uniform
+          const float ds = e4m3_to_f32(b);
+          f = ds == 0.0f ? 0.0f : __fdiv_rn(dd.tsf, ds);
+        } else {
+          f = tk_factor(tabs + dd.tab, b);
+        }
+        const float2 ff = make_float2(f, f);
+        float2 z[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) z[m] = __fmul2_rn(y[m], ff);
+        if (has) st_global_v2(dd.out + el_off, e2m1_word(z[0], z[1], z[2], z[3]), e2m1_word(z[4], z[5], z[6], z[7]));
+        if (has_scale) st_global_u8(dd.scale + sc_off, b);
+      }
+    } else {
+      const MxScale sc = mx_scale<FMT == kMXFP4 ? 6 : 448>(amax);
+      const uint32_t sbyte = has ? sc.byte : 0u;
+      uint32_t o[8];
+      if constexpr (FMT == kMXFP4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[c] = quant8_e2m1_pow2(cur.v[c], sc.pow2);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint2 qq = quant8_e4m3_pow2(cur.v[c], sc.pow2);
+          o[2 * c] = qq.x;
+          o[2 * c + 1] = qq.y;
+        }
+      }
+      const int64_t el_off = static_cast<int64_t>(j) * (FMT == kMXFP4 ? 16 : 32);
+      const bool ov32 = a.out_vec32 != 0;
+#pragma unroll 1
+      for (int i = 0; i < nv; ++i) {
+        uint8_t* dst = desc[i].out + el_off;
+        if (has) {
+          if constexpr (FMT == kMXFP4) {
+            st_global_v4(dst, o[0], o[1], o[2], o[3]);
+          } else if (ov32) {
+            st_global_v8(dst, o);
+          } else {
+            st_global_v4(dst, o[0], o[1], o[2], o[3]);
+            st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
+          }
+        }
+        if (has_scale) st_global_u8(desc[i].scale + sc_off, sbyte);
+      }
+    }
+    cur = nx;
+  }
+}
+
+// Grid: gridDim.x blocks share q.n_tok source rows evenly (block b owns
+// [b n / P, (b+1) n / P)); with no row_indices destination row d reads
+// source row d and n_tok covers every destination row.
+template <int FMT>
+__global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const GroupedArgs a, const TqArgs q) {
+  extern __shared__ __align__(16) uint8_t tq_smem[];
+  TqShared& sh = *reinterpret_cast<TqShared*>(tq_smem);
+  int4* stage = reinterpret_cast<int4*>(tq_smem + sizeof(TqShared));  // 2 x stage_ints entries
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(tq_smem + sizeof(TqShared) + static_cast<size_t>(q.stage_ints) * 8);
+  uint32_t* bkt = cnt + q.tpb;
+  float* tabs = reinterpret_cast<float*>(bkt + static_cast<int64_t>(q.tpb) * kTqBucket);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t_lo = static_cast<int64_t>(blockIdx.x) * q.n_tok / gridDim.x;
+  const int64_t t_hi = static_cast<int64_t>(blockIdx.x + 1) * q.n_tok / gridDim.x;
+  const int nt = static_cast<int>(t_hi - t_lo);
+  const bool gather = a.row_indices != nullptr;
+  if constexpr (FMT == kNVFP4) fill_div6_table(sh.div6_tab, threadIdx.x, kTqThreads);
+  for (int i = threadIdx.x; i < nt; i += kTqThreads) cnt[i] = 0u;
+  // row_indices: a scalar head up to its first 16-byte boundary, a 16-byte
+  // body staged into shared memory by bulk copies (chunks of stage_ints
+  // entries, two buffers), a scalar tail.  All total_rows entries are
+  // staged; only those below min(row_offsets[G], total_rows) are filed.
+  const int64_t mis = gather ? static_cast<int64_t>(((16 - (reinterpret_cast<uintptr_t>(a.row_indices) & 15)) & 15) >> 2) : 0;
+  const int64_t head = mis < a.total_rows ? mis : a.total_rows;
+  const int64_t nvec = gather ? (a.total_rows - head) >> 2 : 0;   // 16-byte vectors in the body
+  const int64_t cvec = q.stage_ints >> 2;                         // vectors per chunk
+  const int64_t n_chunks = (nvec + cvec - 1) / cvec;
+  const int4* body = reinterpret_cast<const int4*>(a.row_indices + head);
+  auto chunk_bytes = [&](int64_t c) { return static_cast<uint32_t>(min(cvec, nvec - c * cvec) * 16); };
+  if (threadIdx.x == 0) {
+    sh.heavy = 0u;
+    sh.failed = 0u;
+    mbar_init(&sh.stage_bar[0], 1);
+    mbar_init(&sh.stage_bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    for (int64_t c = 0; c < 2 && c < n_chunks; ++c) {
+      mbar_arrive_expect_tx(&sh.stage_bar[c], chunk_bytes(c));
+      bulk_load(stage + c * cvec, body + c * cvec, chunk_bytes(c), &sh.stage_bar[c]);
+    }
+  }
+
+  // the first step of each warp's first token row, in flight during the scan
+  TqChunk<FMT> pre;
+  tq_zero(pre);
+  if (warp < nt && t_lo + warp < a.in_rows && lane < a.K / Fmt<FMT>::SF)
+    tq_load(pre, a.in + (t_lo + warp) * a.ld_in + Fmt<FMT>::SF * lane, a.in_vec32 != 0);
+
+  if (blockIdx.x == 0 && threadIdx.x == 0) check_offsets(a);
+  for (int i = threadIdx.x; i <= a.G; i += kTqThreads) {
+    sh.ro[i] = __ldg(a.row_offsets + i);
+    sh.so[i] = __ldg(a.scales_offsets + i);
+    if (i < a.G) sh.e[i] = __ldg(a.expert_ids + i);
+  }
+  if constexpr (FMT == kNVFP4) {
+    for (int i = threadIdx.x; i < q.n_tab * 16; i += kTqThreads) {
+      const int m = i & 15;
+      tabs[i] = m == 0 ? 0.0f : __fdiv_rn(__ldg(a.sf + (i >> 4)), static_cast<float>(m));
+    }
+  }
+  __syncthreads();
+  const int64_t ro_end = sh.ro[a.G];
+  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+
+  // (1) scan: file the destination rows of this block's tokens.  Every
+  // block reads every entry, so the per-entry test is kept to a 32-bit
+  // subtract and compare (source rows and in_rows are below 2^31); only
+  // block 0 also looks for source rows outside x, which it reports.
+  int64_t done = 0;                              // staged chunks filed
+  int64_t issued = n_chunks < 2 ? n_chunks : 2;  // staged chunks copied
+  if (gather) {
+    const uint32_t t_lo32 = static_cast<uint32_t>(t_lo), nt32 = static_cast<uint32_t>(nt);
+    const bool reporter = blockIdx.x == 0;
+    auto file = [&](int64_t d, int32_t src) {
+      const uint32_t k = static_cast<uint32_t>(src) - t_lo32;
+      if (k < nt32) {
+        const uint32_t slot = atomicAdd(&cnt[k], 1u);
+        if (slot < kTqBucket) bkt[k * kTqBucket + slot] = static_cast<uint32_t>(d);
+      } else if (reporter && (src < 0 || src >= a.in_rows)) {
+        int64_t sr;
+        int e;
+        tq_check(a, sh, d, src, sr, e);  // reports the bad source row of a kept group
+      }
+    };
+    if (threadIdx.x < 8) {
+      const int64_t d = threadIdx.x < 4 ? threadIdx.x : head + 4 * nvec + (threadIdx.x - 4);
+      if ((threadIdx.x < 4 ? d < head : true) && d < rows) file(d, __ldg(a.row_indices + d));
+    }
+    // staged body vectors holding rows below `rows` (the scalar tail holds the rest)
+    const int64_t rows_vec = min(nvec, rows > head ? (rows - head + 3) >> 2 : int64_t(0));
+#pragma unroll 1
+    for (int64_t c = 0; c < n_chunks && c * cvec < rows_vec; ++c) {
+      const int b = static_cast<int>(c & 1);
+      if (!mbar_wait_bounded(&sh.stage_bar[b], static_cast<uint32_t>((c >> 1) & 1))) {
+        record_error(kErrTimeout);
+        sh.failed = 1u;
+      }
+      if (!__syncthreads_or(sh.failed != 0u)) {
+        const int4* buf = stage + b * cvec;
+        const int64_t v0 = c * cvec;
+        const int nv = static_cast<int>(min(cvec, rows_vec - v0));  // vectors of this chunk with rows to file
+        const int nfull = static_cast<int>(max(int64_t(0), min(static_cast<int64_t>(nv), (rows - head) / 4 - v0)));  // all 4 below rows
+        const uint32_t d0 = static_cast<uint32_t>(head + 4 * v0);
+        for (int v = threadIdx.x; v < nfull; v += kTqThreads) {
+          const int4 qv = buf[v];
+          const uint32_t d = d0 + 4u * static_cast<uint32_t>(v);
+          file(d, qv.x);
+          file(d + 1, qv.y);
+          file(d + 2, qv.z);
+          file(d + 3, qv.w);
+        }
+        for (int v = nfull + static_cast<int>(threadIdx.x); v < nv; v += kTqThreads) {
+          const int4 qv = buf[v];
+          const int64_t d = head + 4 * (v0 + v);
+          if (d < rows) file(d, qv.x);
+          if (d + 1 < rows) file(d + 1, qv.y);
+          if (d + 2 < rows) file(d + 2, qv.z);
+          if (d + 3 < rows) file(d + 3, qv.w);
+        }
+      }
+      __syncthreads();  // buffer b is free again
+      if (c + 2 < n_chunks) {
+        if (threadIdx.x == 0) {
+          mbar_arrive_expect_tx(&sh.stage_bar[b], chunk_bytes(c + 2));
+          bulk_load(stage + b * cvec, body + (c + 2) * cvec, chunk_bytes(c + 2), &sh.stage_bar[b]);
+        }
+        issued = c + 3;
+      }
+      done = c + 1;
+    }
+  }
+  // chunks [done, issued) were copied but not consumed (rows past
+  // min(row_offsets[G], total_rows), or an expired wait): their copies land
+  // before the block may exit
+  if (threadIdx.x == 0) {
+    for (int64_t c = done; c < issued; ++c)
+      if (!mbar_wait_bounded(&sh.stage_bar[c & 1], static_cast<uint32_t>((c >> 1) & 1))) record_error(kErrTimeout);
+  }
+  __syncthreads();
+  if (sh.failed != 0u) return;  // block-uniform; reported as BSQ_ERR_TIMEOUT
+
+  // (2) + (3): warp w takes tokens w, w + 32, ...
+  const float* div6 = sh.div6_tab;
+  TqDesc* desc = sh.desc[warp];
+#pragma unroll 1
+  for (int k = warp; k < nt; k += kTqWarps) {
+    const int64_t t = t_lo + k;
+    int n;
+    int64_t d = -1;
+    if (gather) {
+      n = static_cast<int>(cnt[k]);
+      if (n > kTqBucket) {  // warp-uniform: left to the re-scan
+        if (lane == 0) sh.heavy = 1u;
+        continue;
+      }
+      if (lane < n) d = bkt[k * kTqBucket + lane];
+    } else {
+      n = t < rows ? 1 : 0;
+      d = t;
+    }
+    const int nv = tq_describe<FMT>(a, sh, desc, lane < n, d, t, q.n_tab);
+    if (nv == 0) continue;  // warp-uniform
+    if (k != warp) {
+      tq_zero(pre);
+      if (lane < a.K / Fmt<FMT>::SF) tq_load(pre, a.in + t * a.ld_in + Fmt<FMT>::SF * lane, a.in_vec32 != 0);
+    }
+    tq_row<FMT>(a, a.in + t * a.ld_in, pre, 0, a.kt_atoms * 4, desc, nv, div6, tabs);
+    __syncwarp();
+  }
+
+  // (4) tokens with more destination rows than a bucket holds: re-scan and
+  // quantize each of their rows on its own (warp-collective).
+  __syncthreads();
+  if (!gather || sh.heavy == 0u) return;  // block-uniform
+#pragma unroll 1
+  for (int64_t d0 = 0; d0 < rows; d0 += kTqThreads) {
+    const int64_t dm = d0 + threadIdx.x;
+    int32_t src = 0;
+    bool hit = false;
+    if (dm < rows) {
+      src = __ldg(a.row_indices + dm);
+      const int64_t k = src - t_lo;
+      hit = k >= 0 && k < nt && cnt[k] > static_cast<uint32_t>(kTqBucket);
+    }
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, hit);
+    while (m != 0u) {
+      const int l = __ffs(m) - 1;
+      m &= m - 1u;
+      const int64_t dd = __shfl_sync(0xFFFFFFFFu, dm, l);
+      const int32_t ss = __shfl_sync(0xFFFFFFFFu, src, l);
+      const int nv = tq_describe<FMT>(a, sh, desc, lane == 0, dd, ss, q.n_tab);
+      if (nv == 0) continue;  // warp-uniform
+      TqChunk<FMT> c;
+      tq_zero(c);
+      if (lane < a.K / Fmt<FMT>::SF)
+        tq_load(c, a.in + static_cast<int64_t>(ss) * a.ld_in + Fmt<FMT>::SF * lane, a.in_vec32 != 0);
+      tq_row<FMT>(a, a.in + static_cast<int64_t>(ss) * a.ld_in, c, 0, a.kt_atoms * 4, desc, nv, div6, tabs);
+      __syncwarp();
+    }
+  }
+}
+
+}  // namespace bsq

@@ -172,7 +172,8 @@ typedef enum {
   BSQ_GROUPED_LATENCY = 2, /* one warp per 2 destination rows (groups of a few rows) */
   BSQ_GROUPED_TOKEN = 3    /* token-major: each source row read once and quantized into all of
                               its destination rows (gathers that reuse source rows, e.g. top-k
-                              routing); needs G <= 1024, else STREAM runs */
+                              routing); one block per SM, each scanning row_indices; needs
+                              G <= 1024 and total_rows < 2^32, else STREAM runs */
 } bsq_grouped_kernel;
 
 /*
