@@ -227,7 +227,8 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
     when ``out`` / ``scales`` are not given).  ``kernel``: "auto", "stream"
     (groups of many rows), "latency" (groups of a few rows) or "token" (a
     row_indices gather that reuses source rows: each read once); the results
-    do not depend on it.
+    do not depend on it.  ``k_tiles_per_block``: 1, 2, 4, 8, or 0 (chosen by
+    the library).
     Returns (packed uint8 (total_rows, packed_row_bytes), scales uint8).
     """
     if kernel not in GROUPED_KERNELS:

@@ -260,6 +260,21 @@ bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t
     kernel = BSQ_GROUPED_STREAM;
   if (kernel == BSQ_GROUPED_TOKEN) return launch_grouped_token<FMT>(a, stream);
   if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_band<FMT>(a, stream);
+  if (kt == 0) {
+    // automatic: the fewest atom columns per unit that still keep the grid
+    // within four blocks per SM (fewer, larger units cost less to schedule
+    // at decode sizes; more blocks than that gave nothing in the k sweeps)
+    DeviceInfo* d = nullptr;
+    if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+    const int64_t row_blocks = ceil_div(a.total_rows, static_cast<int64_t>(kGrWarps) * kRowsPerWarp);
+    kt = 8;
+    for (int c : {1, 2, 4}) {
+      if (row_blocks * ceil_div(a.kt_atoms, c) <= 4 * static_cast<int64_t>(d->sm_count)) {
+        kt = c;
+        break;
+      }
+    }
+  }
   switch (kt) {
     case 1: return launch_grouped_rows<FMT, 1>(a, stream);
     case 2: return launch_grouped_rows<FMT, 2>(a, stream);
@@ -444,7 +459,7 @@ int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows
                                     int64_t total_scale_rows, void* out, void* scales,
                                     int32_t k_tiles_per_block, int32_t kernel, void* stream) {
   if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
-  if (k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
+  if (k_tiles_per_block != 0 && k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
       k_tiles_per_block != 8)
     return BSQ_ERR_VALUE;
   if (kernel != BSQ_GROUPED_AUTO && kernel != BSQ_GROUPED_STREAM && kernel != BSQ_GROUPED_LATENCY &&

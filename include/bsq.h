@@ -146,9 +146,11 @@ BSQ_API int32_t bsq_quantize(int32_t fmt, const void* in_dev, int64_t M, int64_t
  *                       columns 0x00); padding rows are not written.
  *   k_tiles_per_block   1, 2, 4 or 8 column tiles (64 columns for NVFP4, 128
  *                       for MX) handled by one unit of work of the latency
- *                       kernel (a warp); the streaming kernel's thread blocks
- *                       take fixed runs of 7168 columns.  Results do not
- *                       depend on it.
+ *                       kernel (a warp), or 0: chosen by the library (the
+ *                       fewest that keep the latency kernel's grid within
+ *                       four blocks per SM, else 8); the streaming kernel's
+ *                       thread blocks take fixed runs of 7168 columns.
+ *                       Results do not depend on it.
  * Device checks (error word BSQ_ERR_VALUE, the affected rows are skipped):
  * a source row index outside [0, in_rows); row_offsets[G] > total_rows;
  * scales_offsets[G] > total_scale_rows; scales_offsets[0] != 0; a group with

@@ -33,3 +33,20 @@ def guarded(nbytes: int, device="cuda"):
 def margin_intact(full) -> bool:
     tail = full[-MARGIN:].cpu().numpy()
     return bool(np.all(tail == SENTINEL))
+
+
+def _oracle_rank2_job(job):
+    """Process-pool task: the oracle's quantize_rank2 of one chunk of rows."""
+    import oracle
+    fmt, bits, tsf = job
+    return oracle.quantize_rank2(fmt, bits, tsf)
+
+
+def oracle_rank2_chunks(fmt, jobs):
+    """oracle.quantize_rank2 over a list of (bits, tsf) jobs, spread over a
+    spawned process pool (one worker per host core): [(packed, scales2d)]."""
+    import multiprocessing as mp
+    import os
+    from concurrent.futures import ProcessPoolExecutor
+    with ProcessPoolExecutor(max_workers=max(1, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as pool:
+        return list(pool.map(_oracle_rank2_job, [(fmt, b, t) for b, t in jobs], chunksize=1))

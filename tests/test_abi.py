@@ -103,7 +103,8 @@ def g(lib, fmt=0, inp=P, in_rows=64, K=256, ld=256, ro=P, so=P, eid=P, sf=P, ne=
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(fmt=5), VALUE), (dict(kt=3), VALUE), (dict(kt=0), VALUE), (dict(kt=16), VALUE),
+    (dict(fmt=5), VALUE), (dict(kt=3), VALUE), (dict(kt=-1), VALUE), (dict(kt=16), VALUE),
+    (dict(kt=0, G=0), OK),
     (dict(G=-1), VALUE), (dict(G=(1 << 20) + 1), VALUE),
     (dict(K=100, ld=100), SHAPE), (dict(in_rows=-1), SHAPE), (dict(total_rows=-1), SHAPE),
     (dict(total_scale_rows=100), SHAPE), (dict(ld=128), SHAPE),

@@ -156,22 +156,21 @@ FULL = {
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8", "mxfp4"])
-def test_dense_full_size_sampled_rows(bsq, fmt):
+def test_dense_full_size_all_rows(bsq, fmt):
     """The full workloads (NVFP4 8192 x 7168; MXFP8 / MXFP4 16384 x 4096) in
-    the benchmark's launch configuration; the oracle checks 384 sampled rows
-    (first, last, and random) and their scale bytes."""
+    the benchmark's launch configuration: every packed row and every scale
+    byte against the oracle (computed in 512-row chunks over a spawned
+    process pool)."""
+    from bsq_testlib import oracle_rank2_chunks
     c = FULL[fmt]()
     bits, M, K = c["x_bits"], c["M"], c["K"]
     tsf = c["tensor_sf"]
     p, s = _run_dense(bsq, fmt, bits, tsf)
-    rng = np.random.Generator(np.random.PCG64(17))
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, M - 1], rng.choice(M, 379, replace=False)]))
-    p_ref, s_ref = oracle.quantize_rank2(fmt, bits[rows], tsf)
-    np.testing.assert_array_equal(p[rows], p_ref)
-    S = K // oracle.block_size(fmt)
-    Kt = -(-S // 4)
-    mm, ss = np.meshgrid(rows, np.arange(S), indexing="ij")
-    np.testing.assert_array_equal(s[oracle.offset_5d(mm, ss, Kt)], s_ref)
+    refs = oracle_rank2_chunks(fmt, [(bits[r0:r0 + 512], np.float32(tsf)) for r0 in range(0, M, 512)])
+    p_ref = np.concatenate([r[0] for r in refs])
+    s2 = np.concatenate([r[1] for r in refs])
+    np.testing.assert_array_equal(p, p_ref)
+    np.testing.assert_array_equal(s, oracle.scales_to_5d(s2))
 
 
 # ---------------------------------------------------------------- interleave --

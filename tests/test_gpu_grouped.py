@@ -149,39 +149,103 @@ def test_grouped_many_groups_search(bsq):
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
 @pytest.mark.parametrize("K", [7168, 2048])
-@pytest.mark.parametrize("kt", [1, 2, 4, 8])
+@pytest.mark.parametrize("kt", [0, 1, 2, 4, 8])
 @pytest.mark.parametrize("kernel", ["auto", "stream"])
 def test_grouped_decode_full_config(bsq, fmt, K, kt, kernel):
     """Decode: 64 tokens, top-8 over 256 experts (512 rows, many 1-row
-    experts), row_indices gather -- fully compared."""
+    experts), row_indices gather -- fully compared (kt = 0: the library
+    chooses k_tiles_per_block)."""
     d = wl.config_grouped_decode(K=K, fmt=fmt)
     assert d["total_rows"] / d["G"] <= 8
     p, s = _run_grouped(bsq, fmt, d, kt, kernel=kernel)
     _compare(fmt, d, p, s)
 
 
-@pytest.mark.parametrize("kernel", ["auto", "latency", "stream", "token"])
-def test_grouped_prefill_full_config_sampled(bsq, kernel):
-    """Prefill: 4096 tokens, top-8 over 256 experts, K=7168 (32768 rows) at
-    the benchmark's launch configuration; the oracle checks sampled groups
-    (the largest, the smallest and random ones)."""
-    d = wl.config_grouped_prefill()
-    kt = 8
-    p, s = _run_grouped(bsq, "nvfp4", d, kt, kernel=kernel)
-    m = np.diff(d["row_offsets"].astype(np.int64))
-    rng = np.random.Generator(np.random.PCG64(3))
-    groups = np.unique(np.concatenate([[np.argmax(m), np.argmin(m)], rng.choice(d["G"], 10, replace=False)]))
+_PREFILL = {}
+
+
+def _prefill_reference(fmt):
+    """The prefill workload (4096 tokens, top-8 of 256 experts, K = 7168:
+    32768 destination rows) and the oracle's quantization of every group,
+    in row chunks over a spawned process pool; computed once per format."""
+    if fmt not in _PREFILL:
+        from bsq_testlib import oracle_rank2_chunks
+        d = _PREFILL.get("workload")
+        if d is None:
+            d = _PREFILL["workload"] = wl.config_grouped_prefill()
+        ro, eid = d["row_offsets"].astype(np.int64), d["expert_ids"]
+        chunks, jobs = [], []
+        for gi in range(d["G"]):
+            tsf = np.float32(d["sf_tensor"][eid[gi]]) if fmt == "nvfp4" else np.float32(1.0)
+            for r0 in range(int(ro[gi]), int(ro[gi + 1]), 512):
+                r1 = min(r0 + 512, int(ro[gi + 1]))
+                chunks.append((gi, r0, r1))
+                jobs.append((d["x_bits"][d["row_indices"][r0:r1]], tsf))
+        _PREFILL[fmt] = (chunks, oracle_rank2_chunks(fmt, jobs))
+    return _PREFILL["workload"], _PREFILL[fmt]
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("kernel", ["auto", "token", "stream"])
+def test_grouped_prefill_full_config_all_rows(bsq, fmt, kernel):
+    """Prefill at full size (32768 rows, K = 7168) in the benchmark's launch
+    configuration: every packed row and every written scale byte against the
+    oracle, and the padding scale rows (never written) keep their sentinel."""
+    d, (chunks, refs) = _prefill_reference(fmt)
+    p, s = _run_grouped(bsq, fmt, d, 8, kernel=kernel)
     K = d["K"]
-    S = K // 16
+    S = K // oracle.block_size(fmt)
     Kt = -(-S // 4)
-    for gi in groups:
-        r0, r1 = int(d["row_offsets"][gi]), int(d["row_offsets"][gi + 1])
-        e = d["expert_ids"][gi]
-        pd, sd = oracle.quantize_rank2("nvfp4", d["x_bits"][d["row_indices"][r0:r1]], d["sf_tensor"][e])
-        np.testing.assert_array_equal(p[r0:r1], pd)
-        srow = int(d["scales_offsets"][gi]) + np.arange(r1 - r0)
-        mm, ss = np.meshgrid(srow, np.arange(S), indexing="ij")
-        np.testing.assert_array_equal(s[oracle.offset_5d(mm, ss, Kt)], sd)
+    written = np.zeros(s.size, bool)
+    so, ro = d["scales_offsets"].astype(np.int64), d["row_offsets"].astype(np.int64)
+    for (gi, r0, r1), (pd, sd) in zip(chunks, refs):
+        np.testing.assert_array_equal(p[r0:r1], pd, err_msg=f"group {gi} rows {r0}:{r1}")
+        full = np.zeros((r1 - r0, Kt * 4), np.uint8)
+        full[:, :S] = sd
+        srow = so[gi] + (np.arange(r0, r1) - ro[gi])
+        mm, ss = np.meshgrid(srow, np.arange(Kt * 4), indexing="ij")
+        off = oracle.offset_5d(mm, ss, Kt)
+        np.testing.assert_array_equal(s[off], full, err_msg=f"group {gi} scales rows {r0}:{r1}")
+        written[off] = True
+    assert np.all(s[~written] == SENTINEL), "padding scale rows were written"
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("kernel", ["token", "stream", "latency"])
+def test_grouped_source_row_past_a_full_bucket_offset_indices(bsq, fmt, kernel):
+    """row_indices starting 4 bytes past a 16-byte boundary (a scalar head of
+    three entries), a row count that is not a multiple of 4 (a scalar tail),
+    one source row in 40 positions (among them the first three and the last
+    three), one in exactly 16 (a full bucket of the token kernel) and one in
+    17 (one past it): the token kernel's re-scan path and every part of its
+    staged scan, against the oracle."""
+    d = wl.config_grouped_prefill(seed=21, tokens=67, K=256, num_experts=8, top_k=3, fmt=fmt)
+    assert d["total_rows"] % 4 != 0
+    rng = np.random.Generator(np.random.PCG64(22))
+    ridx = d["row_indices"].copy()
+    ridx[np.isin(ridx, [7, 11, 13])] = 5
+    n = ridx.size
+    pos = rng.permutation(np.arange(3, n - 3))
+    heavy = np.concatenate([[0, 1, 2, n - 3, n - 2, n - 1], pos[:34]])
+    ridx[heavy] = 7
+    ridx[pos[34:50]] = 11
+    ridx[pos[50:67]] = 13
+    assert np.sum(ridx == 7) == 40 and np.sum(ridx == 11) == 16 and np.sum(ridx == 13) == 17
+    dev = i32_device(np.concatenate([[0, 0, 0, 0, 7], ridx]))[5:]   # 20 bytes into a 16-byte aligned buffer
+    assert dev.data_ptr() % 16 == 4
+    x_bits = d["x_bits"]
+    total_rows, tsr = d["total_rows"], d["total_scale_rows"]
+    ob = total_rows * oracle.packed_row_bytes(fmt, 256)
+    sb = oracle.scales5d_bytes(tsr, 256 // oracle.block_size(fmt))
+    ofull, out = guarded(ob)
+    sfull, sc = guarded(sb)
+    bsq.grouped_quantize(to_device_bf16(x_bits), fmt, u32_device(d["row_offsets"]), u32_device(d["scales_offsets"]),
+                         i32_device(d["expert_ids"]), torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
+                         dev, total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=2, out=out, scales=sc,
+                         kernel=kernel)
+    assert bsq.device_error() == 0
+    assert margin_intact(ofull) and margin_intact(sfull)
+    _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy(), ridx=ridx)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
