@@ -107,6 +107,9 @@ bsq_status device_info(DeviceInfo** out) {
     dense_kernel_setup<kNVFP4>(0, d);
     dense_kernel_setup<kMXFP4>(1, d);
     dense_kernel_setup<kMXFP8>(2, d);
+    cudaFuncSetAttribute(gemm_quant_kernel<kNVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes());
+    cudaFuncSetAttribute(gemm_quant_kernel<kMXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes());
+    cudaFuncSetAttribute(gemm_quant_kernel<kMXFP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes());
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     d.tq_max_smem = optin;
@@ -231,12 +234,33 @@ bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
+// 2D TMA map of a K-major BF16 operand: rows x K, row stride ld elements,
+// boxes of 64 elements (128 bytes, 128-byte swizzle) x box_rows rows; reads
+// past the edges return zeros.
+bool gemm_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+  auto enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGmBK), box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int FMT>
-bsq_status launch_gemm_quant(const GemmQuantArgs& p, cudaStream_t stream) {
-  const int64_t gy = 2 * ceil_div(p.M, 128);  // every row of the last 128-row band gets its scales
-  if (gy > 65535) return BSQ_ERR_SHAPE;
-  const dim3 grid(static_cast<unsigned>(p.N / kGqBN), static_cast<unsigned>(gy));
-  const cudaError_t e = launch_pdl(gemm_quant_kernel<FMT>, grid, dim3(kGqThreads), 0, stream, p);
+bsq_status launch_gemm_quant(const GemmQuantArgs& p, const void* a, int64_t lda, const void* b, int64_t ldb,
+                             cudaStream_t stream) {
+  DeviceInfo* d = nullptr;
+  if (bsq_status s = device_info(&d); s != BSQ_OK) return s;
+  CUtensorMap ma, mb;
+  if (!gemm_operand_map(&ma, a, p.M, p.K, lda, kGmBM) || !gemm_operand_map(&mb, b, p.N, p.K, ldb, kGmBN))
+    return BSQ_ERR_CUDA;
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, d->sm_count));
+  const cudaError_t e = launch_pdl(gemm_quant_kernel<FMT>, dim3(grid), dim3(kGmThreads), gemm_smem_bytes(), stream,
+                                   ma, mb, p);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -534,14 +558,13 @@ int32_t bsq_gemm_quantize(int32_t fmt, const void* a, const void* b, int64_t M, 
       !aligned(scales5d, 16) || !aligned(c_bf16, 16))
     return BSQ_ERR_ALIGN;
   if (fmt == BSQ_NVFP4 && !(std::isfinite(tensor_sf) && tensor_sf > 0.0f)) return BSQ_ERR_VALUE;
+  if (ceil_div(M, kGmBM) * ceil_div(N, kGmBN) >= (int64_t(1) << 31) || M >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
   GemmQuantArgs p{};
-  p.a = static_cast<const uint16_t*>(a);
-  p.b = static_cast<const uint16_t*>(b);
   p.M = M;
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.lda = lda;
-  p.ldb = ldb;
+  p.tiles_m = static_cast<int>(ceil_div(M, kGmBM));
+  p.tiles_n = static_cast<int>(ceil_div(N, kGmBN));
   p.tsf = fmt == BSQ_NVFP4 ? tensor_sf : 1.0f;
   p.out = static_cast<uint8_t*>(out);
   p.out_ld = row_bytes_of(fmt, N);
@@ -551,9 +574,9 @@ int32_t bsq_gemm_quantize(int32_t fmt, const void* a, const void* b, int64_t M, 
   p.vec32 = aligned(out, 32) && p.out_ld % 32 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (fmt) {
-    case BSQ_NVFP4: return launch_gemm_quant<kNVFP4>(p, st);
-    case BSQ_MXFP4: return launch_gemm_quant<kMXFP4>(p, st);
-    default: return launch_gemm_quant<kMXFP8>(p, st);
+    case BSQ_NVFP4: return launch_gemm_quant<kNVFP4>(p, a, lda, b, ldb, st);
+    case BSQ_MXFP4: return launch_gemm_quant<kMXFP4>(p, a, lda, b, ldb, st);
+    default: return launch_gemm_quant<kMXFP8>(p, a, lda, b, ldb, st);
   }
 }
 

@@ -349,9 +349,10 @@ BSQ_API int32_t bsq_block_scaled_dot(int32_t fmt, const void* a_packed_dev, cons
  *   c_bf16_dev    optional (NULL = none): M x N BF16 copy of C, row stride N,
  *                 16-byte aligned (for checks: the fused bytes equal
  *                 bsq_quantize applied to it).
- * The mainloop is the warp-level tensor-core path (mma.sync), 64 x 64 tiles;
- * errors: BSQ_ERR_SHAPE, BSQ_ERR_NULL, BSQ_ERR_ALIGN, BSQ_ERR_VALUE (format or
- * tensor_sf), BSQ_ERR_CUDA (launch).
+ * The mainloop runs on the tcgen05 tensor cores: 128 x 256 tiles, operands
+ * staged by TMA, FP32 accumulators in tensor memory, one CTA per SM; a wait
+ * that expires records BSQ_ERR_TIMEOUT.  Errors: BSQ_ERR_SHAPE, BSQ_ERR_NULL,
+ * BSQ_ERR_ALIGN, BSQ_ERR_VALUE (format or tensor_sf), BSQ_ERR_CUDA (launch).
  */
 BSQ_API int32_t bsq_gemm_quantize(int32_t fmt, const void* a_dev, const void* b_dev, int64_t M, int64_t N,
                                   int64_t K, int64_t lda, int64_t ldb, float tensor_sf, void* out_dev,
