@@ -63,3 +63,35 @@ def test_fused_epilogue_equals_quantize_of_its_bf16_product(bsq, fmt, M, N, K, l
     # (3) the fused call without storing C gives the same bytes
     out2, sc2 = bsq.gemm_quantize(a, b, fmt, tsf)
     assert torch.equal(out2, out) and torch.equal(sc2, sc)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+def test_fused_epilogue_full_size_persistent_tiles(bsq, fmt):
+    """The benchmark's shape, 8192 x 2048 x 7168: 512 output tiles over the
+    persistent CTAs (several tiles per CTA, both tensor-memory accumulators
+    reused, the stage ring wrapping many times).  Every packed byte and
+    scale byte equals the oracle's quantization of the kernel's own BF16
+    product (in 512-row chunks over a spawned process pool), and sampled
+    rows of that product match FP64 within the FP32-accumulation bound."""
+    from bsq_testlib import oracle_rank2_chunks
+    c_cfg = wl.config_dense_nvfp4_large()
+    bits = c_cfg["x_bits"]
+    M, K, N = 8192, 7168, 2048
+    x = to_device_bf16(bits)
+    a, b = x, x[4096:4096 + N]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tsf = 2688.0 / 64.0 if fmt == "nvfp4" else 1.0
+    out, sc = bsq.gemm_quantize(a, b, fmt, tsf, c_out=c)
+    c_bits = c.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert bsq.device_error() == 0
+    refs = oracle_rank2_chunks(fmt, [(c_bits[r0:r0 + 512], np.float32(tsf)) for r0 in range(0, M, 512)])
+    np.testing.assert_array_equal(out.cpu().numpy(), np.concatenate([r[0] for r in refs]))
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.scales_to_5d(np.concatenate([r[1] for r in refs])))
+    rng = np.random.Generator(np.random.PCG64(5))
+    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], rng.choice(M, 60, replace=False)]))
+    a64 = _bf16_to_f64(bits[rows])
+    b64 = _bf16_to_f64(bits[4096:4096 + N])
+    c64 = a64 @ b64.T
+    mag = np.abs(a64) @ np.abs(b64).T
+    err = np.abs(_bf16_to_f64(c_bits[rows]) - c64)
+    assert np.all(err <= 2.0 ** -8 * np.abs(c64) + K * 2.0 ** -23 * mag + 1e-30)
