@@ -81,6 +81,12 @@ __global__ void __launch_bounds__(kDenseThreads)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap);
+      // the first tiles' input into L2 while the previous kernel finishes
+      for (int t = blockIdx.x, i = 0; t < a.num_tiles && i < STAGES; t += gridDim.x, ++i) {
+        const int mt = t / a.tiles_k, col0 = (t - mt * a.tiles_k) * kDenseTileCols;
+        tma_prefetch_2d(&tmap, col0, mt * kDenseTileRows);
+        if (col0 + kDenseBoxCols < a.K) tma_prefetch_2d(&tmap, col0 + kDenseBoxCols, mt * kDenseTileRows);
+      }
       pdl_wait();
       pdl_trigger();
       int stage = 0;

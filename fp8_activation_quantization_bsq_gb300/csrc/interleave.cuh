@@ -26,6 +26,10 @@ __global__ void __launch_bounds__(kIlvThreads)
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int a0 = blockIdx.y * kIlvAtoms;
   const int64_t s0 = static_cast<int64_t>(a0) * 4;
+  // the block's rows into L2 while the previous kernel finishes (L2 is the
+  // point of coherence: a later read after the wait still sees its writes)
+  for (int r = threadIdx.x; r < 128; r += kIlvThreads)
+    if (m0 + r < M && s0 < S) prefetch_l2(in + (m0 + r) * ld + s0);
   pdl_wait();
   pdl_trigger();
 
