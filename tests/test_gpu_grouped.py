@@ -432,3 +432,15 @@ def test_grouped_token_kernel_group_limit(bsq, G):
         p, s = _run_grouped(bsq, fmt, d, 1, kernel="token")
         _compare(fmt, d, p, s)
 
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("tokens,K,top_k,experts", [(1, 32, 1, 1), (5, 64, 3, 4), (300, 32, 2, 8),
+                                                     (77825, 32, 2, 64)])
+def test_token_kernel_shapes(bsq, fmt, tokens, K, top_k, experts):
+    """The token kernel's edge shapes: one token, K = 32 (a partial atom and
+    a single step), more SMs than tokens, and 77825 tokens (more than 512
+    per block on 152 SMs, so the grid grows past one block per SM)."""
+    d = wl.config_grouped_prefill(seed=tokens + K, tokens=tokens, K=K, num_experts=experts, top_k=top_k, fmt=fmt)
+    p, s = _run_grouped(bsq, fmt, d, 1, kernel="token")
+    _compare(fmt, d, p, s)
