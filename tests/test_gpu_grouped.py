@@ -444,3 +444,51 @@ def test_token_kernel_shapes(bsq, fmt, tokens, K, top_k, experts):
     d = wl.config_grouped_prefill(seed=tokens + K, tokens=tokens, K=K, num_experts=experts, top_k=top_k, fmt=fmt)
     p, s = _run_grouped(bsq, fmt, d, 1, kernel="token")
     _compare(fmt, d, p, s)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("K", [96, 2112, 7168])
+@pytest.mark.parametrize("gather", [True, False])
+def test_token_kernel_band_shapes(bsq, fmt, K, gather):
+    """The token kernel on scale bands of every fill: groups of 128, 127,
+    129, 256 and 1 rows (whole, partly filled and single-row bands), an empty
+    group, a skipped group that spans whole bands, and a group with a
+    reserved, unused padding tile; with and without the row_indices gather.
+    Every written byte equals the oracle and every padding scale row keeps
+    its sentinel.  K = 96 / 2112 / 7168 give 1, 33 and 112 (NVFP4) atoms per
+    band row."""
+    rng = np.random.Generator(np.random.PCG64(K + 7 * gather))
+    m = np.array([128, 0, 127, 129, 256, 300, 128, 1], np.int64)
+    tiles = -(-m // 128)
+    tiles[6] += 1                                   # a reserved, unused tile
+    G = m.size
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = np.concatenate([[0], np.cumsum(tiles * 128)]).astype(np.uint32)
+    total_rows = int(ro[-1])
+    in_rows = 300 if gather else total_rows
+    x = wl.dense_activations(rng, in_rows, K, "blocklognormal")
+    ridx = rng.integers(0, in_rows, size=total_rows).astype(np.int32) if gather else None
+    eid = np.array([0, 1, 2, 3, 4, -1, 5, 6], np.int32)
+    sf = (rng.random(7).astype(np.float32) + np.float32(0.5)) * np.float32(100.0)
+    d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=eid, sf_tensor=sf,
+             row_indices=ridx, total_rows=total_rows, total_scale_rows=int(so[-1]), G=G)
+    p, s = _run_grouped(bsq, fmt, d, 8, use_ridx=gather, kernel="token")
+    _compare(fmt, d, p, s, use_ridx=gather)
+
+
+def test_token_kernel_wide_rows(bsq):
+    """The token kernel at K = 32768 (NVFP4: 2048 scale blocks, 512 atoms per
+    band row; 64 steps per destination row): a whole band and a 5-row band,
+    bytes equal to the oracle."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    m = np.array([128, 5], np.int64)
+    ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
+    so = np.concatenate([[0], np.cumsum(-(-m // 128) * 128)]).astype(np.uint32)
+    K, in_rows = 32768, 40
+    x = wl.dense_activations(rng, in_rows, K, "normal")
+    ridx = rng.integers(0, in_rows, size=int(ro[-1])).astype(np.int32)
+    d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=np.array([1, 0], np.int32),
+             sf_tensor=np.array([3.0, 0.25], np.float32), row_indices=ridx, total_rows=int(ro[-1]),
+             total_scale_rows=int(so[-1]), G=2)
+    p, s = _run_grouped(bsq, "nvfp4", d, 8, kernel="token")
+    _compare("nvfp4", d, p, s)
