@@ -228,8 +228,38 @@ def time_events(fn, reps: int, flush=None):
     return statistics.mean(ms), min(ms)
 
 
+ROT_SETS = 3        # buffer sets cycled by the back-to-back context timings
+ROT_LAUNCHES = 30
+
+
+def time_rotated(fns, launches: int = ROT_LAUNCHES):
+    """Device ms per launch of ``launches`` launches back to back, cycling
+    through ``fns`` (one per buffer set, each set larger than the L2 or the
+    other sets together larger than it, so that every launch finds its own
+    buffers evicted): one CUDA-event pair on the current stream around all of
+    them, after one untimed launch per set."""
+    import torch
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_hold(1.0 + 0.06 * launches)
+    a.record()
+    for i in range(launches):
+        fns[i % len(fns)]()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / launches
+
+
 def extra_workloads(bsq, device, flush, peak):
-    """The other shapes, reported for context (not the headline)."""
+    """The other shapes, reported for context (not the headline).
+
+    ``us``: device time per launch, launches back to back over ROT_SETS
+    rotated buffer sets (inputs and outputs; cold in L2 for each launch).
+    ``us_single_cold``: one launch between two events after an L2 flush,
+    which adds the launch latency the back-to-back timing hides (about
+    4-5 us on this GPU for a one-block kernel)."""
     import torch
     import workloads as wl
     res = {}
@@ -239,29 +269,39 @@ def extra_workloads(bsq, device, flush, peak):
     x = to_dev_bf16(c["x_bits"], device)
     out, sc = bsq.quantize(x, "nvfp4", float(c["tensor_sf"]))
     mean, mn = time_events(lambda: bsq.quantize(x, "nvfp4", float(c["tensor_sf"]), out=out, scales=sc), reps, flush)
-    res["nvfp4_dense_M128_K256"] = {"us": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
-                                    "GB_s": round(dense_bytes("nvfp4", 128, 256) / (mean * 1e6), 1)}
+    res["nvfp4_dense_M128_K256"] = {"us_single_cold": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
+                                    "GB_s": round(dense_bytes("nvfp4", 128, 256) / (mean * 1e6), 1),
+                                    "note": "one 128-row tile: launch latency"}
 
     # tensor-scale reduction and the on-device NVFP4 chain (tensor_sf, then
     # quantize reading it from device memory) on the 8192 x 7168 activations
     c = wl.config_dense_nvfp4_large()
-    x = to_dev_bf16(c["x_bits"], device)
+    x0 = to_dev_bf16(c["x_bits"], device)
     M, K = c["x_bits"].shape
     del c
+    xs = [x0] + [x0.clone() for _ in range(ROT_SETS - 1)]
     ws = torch.zeros(bsq.lib().bsq_tensor_sf_workspace_bytes(), dtype=torch.uint8, device=device)
-    tsf = bsq.tensor_sf(x, workspace=ws)
-    mean, mn = time_events(lambda: bsq.tensor_sf(x, out=tsf, workspace=ws), reps, flush)
-    res[f"tensor_sf_M{M}_K{K}"] = {"us": round(mean * 1e3, 2), "GB_s": round(M * K * 2 / (mean * 1e6), 1),
-                                   "frac_of_hbm": round(M * K * 2 / (mean * 1e6) / peak, 3)}
-    out, sc = bsq.quantize_dynamic(x, "nvfp4", tsf[1:])
+    tsfs = [bsq.tensor_sf(x, workspace=ws) for x in xs]
+    fns = [lambda x=x, t=t: bsq.tensor_sf(x, out=t, workspace=ws) for x, t in zip(xs, tsfs)]
+    rot = time_rotated(fns)
+    single, _ = time_events(fns[0], reps, flush)
+    res[f"tensor_sf_M{M}_K{K}"] = {"us": round(rot * 1e3, 2), "GB_s": round(M * K * 2 / (rot * 1e6), 1),
+                                   "frac_of_hbm": round(M * K * 2 / (rot * 1e6) / peak, 3),
+                                   "us_single_cold": round(single * 1e3, 2)}
+    outs = [bsq.quantize_dynamic(x, "nvfp4", t[1:]) for x, t in zip(xs, tsfs)]
 
-    def chain():
-        bsq.tensor_sf(x, out=tsf, workspace=ws)
-        bsq.quantize_dynamic(x, "nvfp4", tsf[1:], out=out, scales=sc)
-    mean, mn = time_events(chain, reps, flush)
+    def chain(i):
+        bsq.tensor_sf(xs[i], out=tsfs[i], workspace=ws)
+        bsq.quantize_dynamic(xs[i], "nvfp4", tsfs[i][1:], out=outs[i][0], scales=outs[i][1])
+    rot = time_rotated([lambda i=i: chain(i) for i in range(ROT_SETS)])
+    single, _ = time_events(lambda: chain(0), reps, flush)
     res[f"nvfp4_dynamic_chain_M{M}_K{K}"] = {
-        "us": round(mean * 1e3, 2), "note": "tensor_sf + quantize_dynamic; the input is read twice",
-        "GB_s_of_quantize_bytes": round(dense_bytes("nvfp4", M, K) / (mean * 1e6), 1)}
+        "us": round(rot * 1e3, 2), "us_single_cold": round(single * 1e3, 2),
+        "note": "tensor_sf + quantize_dynamic; the input is read twice",
+        "GB_s_of_quantize_bytes": round(dense_bytes("nvfp4", M, K) / (rot * 1e6), 1)}
+    del outs, tsfs
+    x = xs[0]
+    del xs
 
     # the naive block-scaled matmul validator (FP64 CUDA cores), NVFP4
     # 512 x 512 x 7168 from the first rows of the dense workload
@@ -287,88 +327,107 @@ def extra_workloads(bsq, device, flush, peak):
     res["nvfp4_gemm_quantize_epilogue_8192x2048x7168"] = {
         "us": round(mean * 1e3, 1), "TFLOP_s_bf16": round(tflops, 1),
         "frac_of_bf16_peak": round(tflops / bf16_peak()[0], 3), "bf16_peak_source": bf16_peak()[1],
-        "separate_quantize_of_C_us": round(qmean * 1e3, 2),
-        "note": "tcgen05 mainloop (TMA operands, TMEM accumulators); the epilogue replaces a BF16 C store plus a quantize pass"}
-    del gq, gs, qa, qs, cb, wgt, x, out, sc
+        "separate_quantize_of_C_us_single_cold": round(qmean * 1e3, 2),
+        "note": "tcgen05 mainloop (TMA operands, TMEM accumulators); the epilogue replaces a BF16 C store plus a "
+                "quantize pass; one launch between events after an L2 flush"}
+    del gq, gs, qa, qs, cb, wgt, x
 
     c = wl.config_dense_mx_wide()
-    x = to_dev_bf16(c["x_bits"], device)
+    x0 = to_dev_bf16(c["x_bits"], device)
     del c
+    xs = [x0] + [x0.clone() for _ in range(ROT_SETS - 1)]
     for fmt in ("mxfp8", "mxfp4"):
-        out, sc = bsq.quantize(x, fmt)
-        mean, mn = time_events(lambda: bsq.quantize(x, fmt, out=out, scales=sc), reps, flush)
+        outs = [bsq.quantize(x, fmt) for x in xs]
+        fns = [lambda x=x, o=o: bsq.quantize(x, fmt, out=o[0], scales=o[1]) for x, o in zip(xs, outs)]
+        rot = time_rotated(fns)
+        single, _ = time_events(fns[0], reps, flush)
         b = dense_bytes(fmt, 16384, 4096)
-        res[f"{fmt}_dense_M16384_K4096"] = {"GB_s": round(b / (mean * 1e6), 1), "us": round(mean * 1e3, 2),
-                                            "frac_of_hbm": round(b / (mean * 1e6) / peak, 3)}
-        del out, sc
-    del x
+        res[f"{fmt}_dense_M16384_K4096"] = {"GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
+                                            "frac_of_hbm": round(b / (rot * 1e6) / peak, 3),
+                                            "us_single_cold": round(single * 1e3, 2)}
+        del outs, fns
+    del xs, x0
 
-    def grouped(d, fmt, kt, label, unique_rows, warm=False):
-        xg = to_dev_bf16(d["x_bits"], device)
+    def grouped_sets(d, fmt, kt, sets):
+        """Launch closures over `sets` buffer sets (token-matrix copy, packed
+        output, 5D scales; the metadata shared) and the algorithmic bytes."""
+        x0 = to_dev_bf16(d["x_bits"], device)
+        xgs = [x0] + [x0.clone() for _ in range(sets - 1)]
         u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
         ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
         eid = torch.from_numpy(d["expert_ids"]).to(device)
-        sf = torch.from_numpy(d["sf_tensor"]).to(device)
+        sf = torch.from_numpy(d["sf_tensor"]).to(device) if fmt == "nvfp4" else None
         ridx = torch.from_numpy(d["row_indices"]).to(device)
-        out, sc = bsq.grouped_quantize(xg, fmt, ro, so, eid, sf if fmt == "nvfp4" else None, ridx,
-                                       total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"],
-                                       k_tiles_per_block=kt)
-        fn = lambda: bsq.grouped_quantize(xg, fmt, ro, so, eid, sf if fmt == "nvfp4" else None, ridx,
-                                          total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"],
-                                          k_tiles_per_block=kt, out=out, scales=sc)
-        mean, mn = time_events(fn, reps, flush)
-        warm_ms = time_events(fn, reps)[0] if warm else None
+        kw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=kt)
+        fns = []
+        for xg in xgs:
+            out, sc = bsq.grouped_quantize(xg, fmt, ro, so, eid, sf, ridx, **kw)
+            fns.append(lambda xg=xg, out=out, sc=sc: bsq.grouped_quantize(xg, fmt, ro, so, eid, sf, ridx, out=out,
+                                                                          scales=sc, **kw))
         K = d["K"]
         sfv = 16 if fmt == "nvfp4" else 32
         kt_cols = -(-(K // sfv) // 4) * 4
-        b = (unique_rows * K * 2 + d["total_rows"] * (K if fmt == "mxfp8" else K // 2)
+        uniq = int(np.unique(d["row_indices"]).size)
+        b = (uniq * K * 2 + d["total_rows"] * (K if fmt == "mxfp8" else K // 2)
              + d["total_rows"] * kt_cols + d["row_indices"].nbytes + d["row_offsets"].nbytes
              + d["scales_offsets"].nbytes + d["expert_ids"].nbytes
              + (d["sf_tensor"].nbytes if fmt == "nvfp4" else 0))
-        return (mean, mn, b, warm_ms) if warm else (mean, mn, b)
+        return fns, b
 
     d = wl.config_grouped_prefill()
-    uniq = int(np.unique(d["row_indices"]).size)
-    xg = to_dev_bf16(d["x_bits"], device)
+    x0 = to_dev_bf16(d["x_bits"], device)
+    xgs = [x0] + [x0.clone() for _ in range(ROT_SETS - 1)]
     ro = torch.from_numpy(np.ascontiguousarray(d["row_offsets"], np.uint32).view(np.int32)).to(device)
     eid = torch.from_numpy(d["expert_ids"]).to(device)
     ridx = torch.from_numpy(d["row_indices"]).to(device)
     E = d["num_experts"]
     gws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device=device)
-    gsf = bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], workspace=gws)
-    mean, mn = time_events(lambda: bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"],
-                                                         out=gsf, workspace=gws), reps, flush)
-    res["grouped_tensor_sf_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2),
-                                                    "gathered_GB_s": round(d["total_rows"] * d["K"] * 2 / (mean * 1e6), 1)}
+    gsfs = [bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], workspace=gws) for xg in xgs]
+    fns = [lambda xg=xg, g=g: bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], out=g,
+                                                    workspace=gws) for xg, g in zip(xgs, gsfs)]
+    rot = time_rotated(fns)
+    single, _ = time_events(fns[0], reps, flush)
+    res["grouped_tensor_sf_prefill_T4096_K7168"] = {
+        "us": round(rot * 1e3, 2), "us_single_cold": round(single * 1e3, 2),
+        "gathered_GB_s": round(d["total_rows"] * d["K"] * 2 / (rot * 1e6), 1)}
     # the grouped dynamic chain: per-expert scales on the GPU, then the
     # grouped NVFP4 quantize reading them from device memory
     so_d = torch.from_numpy(np.ascontiguousarray(d["scales_offsets"], np.uint32).view(np.int32)).to(device)
     gkw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=8)
-    go, gsc = bsq.grouped_quantize(xg, "nvfp4", ro, so_d, eid, gsf, ridx, **gkw)
+    gouts = [bsq.grouped_quantize(xg, "nvfp4", ro, so_d, eid, g, ridx, **gkw) for xg, g in zip(xgs, gsfs)]
 
-    def gchain():
-        bsq.grouped_tensor_sf(xg, ro, eid, E, ridx, total_rows=d["total_rows"], out=gsf, workspace=gws)
-        bsq.grouped_quantize(xg, "nvfp4", ro, so_d, eid, gsf, ridx, out=go, scales=gsc, **gkw)
-    mean, mn = time_events(gchain, reps, flush)
-    res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(mean * 1e3, 2)}
-    del go, gsc, so_d
-    del xg, gsf, gws
+    def gchain(i):
+        bsq.grouped_tensor_sf(xgs[i], ro, eid, E, ridx, total_rows=d["total_rows"], out=gsfs[i], workspace=gws)
+        bsq.grouped_quantize(xgs[i], "nvfp4", ro, so_d, eid, gsfs[i], ridx, out=gouts[i][0], scales=gouts[i][1],
+                             **gkw)
+    rot = time_rotated([lambda i=i: gchain(i) for i in range(ROT_SETS)])
+    single, _ = time_events(lambda: gchain(0), reps, flush)
+    res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(rot * 1e3, 2),
+                                                             "us_single_cold": round(single * 1e3, 2)}
+    del gouts, so_d, xgs, x0, gsfs, gws, fns
     for fmt in ("nvfp4", "mxfp8", "mxfp4"):
-        mean, mn, b = grouped(d, fmt, 8, "prefill", uniq)
+        fns, b = grouped_sets(d, fmt, 8, ROT_SETS)
+        rot = time_rotated(fns)
+        single, _ = time_events(fns[0], reps, flush)
         res[f"{fmt}_grouped_prefill_T4096_K7168"] = {
-            "GB_s": round(b / (mean * 1e6), 1), "us": round(mean * 1e3, 2),
-            "frac_of_hbm": round(b / (mean * 1e6) / peak, 3), "algorithmic_bytes": b,
-            "logical_input_bytes": d["total_rows"] * d["K"] * 2,
-            "T_elements_per_s": round(d["total_rows"] * d["K"] / (mean * 1e-3) / 1e12, 2)}
+            "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
+            "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
+            "algorithmic_bytes": b, "logical_input_bytes": d["total_rows"] * d["K"] * 2,
+            "T_elements_per_s": round(d["total_rows"] * d["K"] / (rot * 1e-3) / 1e12, 2)}
+        del fns
     del d
     for fmt in ("nvfp4", "mxfp8"):
         for K in (7168, 2048):
             d = wl.config_grouped_decode(K=K, fmt=fmt)
-            uniq = int(np.unique(d["row_indices"]).size)
             for kt in (0, 1, 2, 4, 8):  # 0: chosen by the library
-                mean, mn, b, warm = grouped(d, fmt, kt, "decode", uniq, warm=True)
+                fns, b = grouped_sets(d, fmt, kt, 1)
+                mean, mn = time_events(fns[0], reps, flush)
+                warm = time_events(fns[0], reps)[0]
+                b2b = time_rotated(fns)
                 res[f"{fmt}_grouped_decode_T64_K{K}_kt{'auto' if kt == 0 else kt}"] = {
-                    "us": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2), "us_warm_l2": round(warm * 1e3, 2)}
+                    "us_single_cold": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
+                    "us_single_warm_l2": round(warm * 1e3, 2), "us_back_to_back_warm_l2": round(b2b * 1e3, 2)}
+                del fns
     return res
 
 
@@ -526,6 +585,10 @@ def run_ours(args, rank, world, local_rank):
         line["cpu_baseline"] = cpu_baseline(c, tsf)
     if not args.no_extra:
         line["workloads"] = extra_workloads(bsq, device, flush, peak)
+        line["workloads_timing"] = (f"us: device time per launch, {ROT_LAUNCHES} launches back to back cycling "
+                                    f"through {ROT_SETS} buffer sets (inputs and outputs; each launch's own "
+                                    "buffers evicted from L2 by the other sets); us_single_cold: one launch "
+                                    "between events after a 2x-L2 read pass (adds the launch latency)")
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
