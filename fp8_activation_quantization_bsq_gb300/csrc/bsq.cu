@@ -228,6 +228,11 @@ bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
   if (fixed + 8 * 16 > static_cast<size_t>(d->tq_max_smem)) return BSQ_ERR_SHAPE;
   const int64_t room = static_cast<int64_t>((static_cast<size_t>(d->tq_max_smem) - fixed) / 8) & ~int64_t(3);
   q.stage_ints = static_cast<int>(std::min<int64_t>(kTqStageInts, room));
+  // few tokens per block: warps claim (token, step) units, the tokens'
+  // descriptors kept in the staging area once the scan is done
+  q.units = (q.tpb <= kTqUnitTokens &&
+             static_cast<size_t>(q.stage_ints) * 8 >= static_cast<size_t>(q.tpb) * (kTqBucket * sizeof(TqDesc) + 4))
+                ? 1 : 0;
   const size_t smem = tq_smem_bytes(q.tpb, q.n_tab, q.stage_ints);
   const cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)),
                                    dim3(kTqThreads), smem, stream, a, q);

@@ -35,6 +35,11 @@ constexpr int kTqMaxTokens = 512;    // tokens per block at most (more: more blo
 constexpr int kTqMaxGroups = 1024;   // group metadata held in shared memory
 constexpr int kTqTabExperts = 1024;  // NVFP4: experts with a factor table in shared memory
 constexpr int kTqStageInts = 16384;  // row_indices entries per staging buffer at most (64 KB)
+constexpr int kTqScanVec = 1;      // staged row_indices vectors tested per thread at a time
+constexpr int kTqUnitTokens = 16;    // tokens per block at most for claimed (token, step) units
+constexpr int kTqBadList = 64;       // out-of-range source rows block 0 keeps for the check (more: a re-scan)
+static_assert(kTqMaxGroups + 1 <= 2 * kTqThreads && kTqTabExperts <= kTqThreads,
+              "the token kernel's threads hold the metadata in registers during the scan");
 
 // One destination row of the token a warp is quantizing.
 struct alignas(16) TqDesc {
@@ -53,6 +58,10 @@ struct TqShared {
   uint64_t stage_bar[2];  // completion of the two row_indices staging buffers
   uint32_t heavy;         // some token of this block has more rows than its bucket
   uint32_t failed;        // a staging wait expired
+  uint32_t n_bad;         // block 0: source rows outside x seen by the scan
+  uint32_t next_unit;     // runs: the next (token, step) unit to claim
+  uint32_t bad_d[kTqBadList];
+  int32_t bad_src[kTqBadList];
 };
 
 // Launch constants of the token kernel (host-computed).
@@ -61,6 +70,7 @@ struct TqArgs {
   int tpb;        // tokens per block at most (size of the buckets)
   int n_tab;      // NVFP4 experts with a factor table (0: every row divides)
   int stage_ints; // row_indices entries per staging buffer (a multiple of 4)
+  int units;      // warps claim (token, step) units; else warp w takes tokens w, w + 32, ...
 };
 
 // Dynamic shared memory: TqShared, two row_indices staging buffers, the
@@ -184,11 +194,12 @@ __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
 // The warp quantizes the scale blocks [jb, je) of source row in_row (jb a
 // multiple of 32, je <= the row's blocks with a scale byte) into its nv
 // described destination rows, 32 blocks per step, lane l on block jb + l,
-// jb + 32 + l, ...  cur holds the lane's block of the first step.
+// jb + 32 + l, ...  cur holds the lane's block of the first step; on return
+// it holds the lane's block next_jb + l of next_row (zeros without one).
 template <int FMT>
 __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_row, TqChunk<FMT>& cur, int jb,
                                        int je, const TqDesc* desc, int nv, const float* div6_tab,
-                                       const float* tabs) {
+                                       const float* tabs, const uint16_t* next_row = nullptr, int next_jb = 0) {
   constexpr int SF = Fmt<FMT>::SF;
   const int lane = threadIdx.x & 31;
   const int S = a.K / SF;          // blocks with data
@@ -198,7 +209,11 @@ __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_
   for (int j = jb + lane; j - lane < je; j += 32) {
     TqChunk<FMT> nx;
     tq_zero(nx);
-    if (j - lane + 32 < je && j + 32 < S) tq_load(nx, in_row + SF * (j + 32), vec32);
+    if (j - lane + 32 < je) {
+      if (j + 32 < S) tq_load(nx, in_row + SF * (j + 32), vec32);
+    } else if (next_row != nullptr && next_jb + lane < S) {
+      tq_load(nx, next_row + SF * (next_jb + lane), vec32);  // the first step of the warp's next run
+    }
     const bool has = j < S, has_scale = j < S4;
     const int64_t sc_off = static_cast<int64_t>(j >> 2) * 512 + (j & 3);
     uint32_t acc = 0;
@@ -306,6 +321,8 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
   if (threadIdx.x == 0) {
     sh.heavy = 0u;
     sh.failed = 0u;
+    sh.n_bad = 0u;
+    sh.next_unit = kTqWarps;  // warp w starts on unit w
     mbar_init(&sh.stage_bar[0], 1);
     mbar_init(&sh.stage_bar[1], 1);
     fence_mbar_init();
@@ -319,46 +336,63 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
     }
   }
 
-  // the first step of each warp's first token row, in flight during the scan
+  // the first step of each warp's first token row (units: of unit w), in
+  // flight during the scan
+  const int steps = (a.kt_atoms * 4 + 31) / 32;  // 32-block steps per row
   TqChunk<FMT> pre;
   tq_zero(pre);
-  if (warp < nt && t_lo + warp < a.in_rows && lane < a.K / Fmt<FMT>::SF)
-    tq_load(pre, a.in + (t_lo + warp) * a.ld_in + Fmt<FMT>::SF * lane, a.in_vec32 != 0);
+  {
+    const int k0 = q.units ? warp / steps : warp;
+    const int j0 = (q.units ? (warp % steps) * 32 : 0) + lane;
+    if (k0 < nt && t_lo + k0 < a.in_rows && j0 < a.K / Fmt<FMT>::SF)
+      tq_load(pre, a.in + (t_lo + k0) * a.ld_in + Fmt<FMT>::SF * j0, a.in_vec32 != 0);
+  }
 
   if (blockIdx.x == 0 && threadIdx.x == 0) check_offsets(a);
-  for (int i = threadIdx.x; i <= a.G; i += kTqThreads) {
-    sh.ro[i] = __ldg(a.row_offsets + i);
-    sh.so[i] = __ldg(a.scales_offsets + i);
-    if (i < a.G) sh.e[i] = __ldg(a.expert_ids + i);
-  }
-  if constexpr (FMT == kNVFP4) {
-    for (int i = threadIdx.x; i < q.n_tab * 16; i += kTqThreads) {
-      const int m = i & 15;
-      tabs[i] = m == 0 ? 0.0f : __fdiv_rn(__ldg(a.sf + (i >> 4)), static_cast<float>(m));
+  // The group metadata and the expert scales are loaded into registers now
+  // and stored to shared memory after the scan, which needs only
+  // row_offsets[G]: their latency hides behind the row_indices copies.
+  // G <= kTqMaxGroups = kTqThreads, so thread i holds entries i and i + 1024.
+  const int64_t ro_end = static_cast<int64_t>(__ldg(a.row_offsets + a.G));
+  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  uint32_t m_ro[2] = {0u, 0u}, m_so[2] = {0u, 0u};
+  int32_t m_e[2] = {0, 0};
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = static_cast<int>(threadIdx.x) + k * kTqThreads;
+    if (i <= a.G) {
+      m_ro[k] = __ldg(a.row_offsets + i);
+      m_so[k] = __ldg(a.scales_offsets + i);
+      if (i < a.G) m_e[k] = __ldg(a.expert_ids + i);
     }
   }
-  __syncthreads();
-  const int64_t ro_end = sh.ro[a.G];
-  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  // NVFP4: thread e < n_tab (<= kTqTabExperts = kTqThreads) owns expert e's table
+  const float m_sf = (FMT == kNVFP4 && static_cast<int>(threadIdx.x) < q.n_tab) ? __ldg(a.sf + threadIdx.x) : 0.0f;
 
   // (1) scan: file the destination rows of this block's tokens.  Every
-  // block reads every entry, so the per-entry test is kept to a 32-bit
-  // subtract and compare (source rows and in_rows are below 2^31); only
-  // block 0 also looks for source rows outside x, which it reports.
+  // block reads every entry, so the per-entry test is a 32-bit subtract and
+  // compare (source rows and in_rows are below 2^31), four staged vectors
+  // per thread at a time, with the rare hits filed afterwards; block 0 also
+  // notes source rows outside x, which are checked (and reported when their
+  // group is kept) once the metadata is in shared memory.
   int64_t done = 0;                              // staged chunks filed
   int64_t issued = n_chunks < 2 ? n_chunks : 2;  // staged chunks copied
+  const bool reporter = blockIdx.x == 0;
   if (gather) {
     const uint32_t t_lo32 = static_cast<uint32_t>(t_lo), nt32 = static_cast<uint32_t>(nt);
-    const bool reporter = blockIdx.x == 0;
+    // (in_rows >= 2^31: every non-negative int32 source row is inside x)
+    const uint32_t in_rows32 = static_cast<uint32_t>(a.in_rows < 0x80000000LL ? a.in_rows : 0x80000000LL);
     auto file = [&](int64_t d, int32_t src) {
       const uint32_t k = static_cast<uint32_t>(src) - t_lo32;
       if (k < nt32) {
         const uint32_t slot = atomicAdd(&cnt[k], 1u);
         if (slot < kTqBucket) bkt[k * kTqBucket + slot] = static_cast<uint32_t>(d);
-      } else if (reporter && (src < 0 || src >= a.in_rows)) {
-        int64_t sr;
-        int e;
-        tq_check(a, sh, d, src, sr, e);  // reports the bad source row of a kept group
+      } else if (reporter && static_cast<uint32_t>(src) >= in_rows32) {
+        const uint32_t j = atomicAdd(&sh.n_bad, 1u);
+        if (j < kTqBadList) {
+          sh.bad_d[j] = static_cast<uint32_t>(d);
+          sh.bad_src[j] = src;
+        }
       }
     };
     if (threadIdx.x < 8) {
@@ -380,13 +414,39 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
         const int nv = static_cast<int>(min(cvec, rows_vec - v0));  // vectors of this chunk with rows to file
         const int nfull = static_cast<int>(max(int64_t(0), min(static_cast<int64_t>(nv), (rows - head) / 4 - v0)));  // all 4 below rows
         const uint32_t d0 = static_cast<uint32_t>(head + 4 * v0);
-        for (int v = threadIdx.x; v < nfull; v += kTqThreads) {
-          const int4 qv = buf[v];
-          const uint32_t d = d0 + 4u * static_cast<uint32_t>(v);
-          file(d, qv.x);
-          file(d + 1, qv.y);
-          file(d + 2, qv.z);
-          file(d + 3, qv.w);
+#pragma unroll 1
+        for (int v = threadIdx.x; v < nfull; v += kTqScanVec * kTqThreads) {
+          int4 qv[kTqScanVec];
+          bool in[kTqScanVec];
+#pragma unroll
+          for (int j = 0; j < kTqScanVec; ++j) {
+            in[j] = v + j * kTqThreads < nfull;
+            qv[j] = in[j] ? buf[v + j * kTqThreads] : make_int4(0, 0, 0, 0);
+          }
+          uint32_t hit = 0u;
+#pragma unroll
+          for (int j = 0; j < kTqScanVec; ++j) {
+            const uint32_t s4[4] = {static_cast<uint32_t>(qv[j].x), static_cast<uint32_t>(qv[j].y),
+                                    static_cast<uint32_t>(qv[j].z), static_cast<uint32_t>(qv[j].w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool h = s4[e] - t_lo32 < nt32 || (reporter && s4[e] >= in_rows32);
+              hit |= (in[j] && h) ? (1u << (4 * j + e)) : 0u;
+            }
+          }
+          if (hit != 0u) {
+#pragma unroll
+            for (int j = 0; j < kTqScanVec; ++j) {
+              const uint32_t h = (hit >> (4 * j)) & 15u;
+              if (h != 0u) {
+                const uint32_t d = d0 + 4u * static_cast<uint32_t>(v + j * kTqThreads);
+                if (h & 1u) file(d, qv[j].x);
+                if (h & 2u) file(d + 1, qv[j].y);
+                if (h & 4u) file(d + 2, qv[j].z);
+                if (h & 8u) file(d + 3, qv[j].w);
+              }
+            }
+          }
         }
         for (int v = nfull + static_cast<int>(threadIdx.x); v < nv; v += kTqThreads) {
           const int4 qv = buf[v];
@@ -415,14 +475,116 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
     for (int64_t c = done; c < issued; ++c)
       if (!mbar_wait_bounded(&sh.stage_bar[c & 1], static_cast<uint32_t>((c >> 1) & 1))) record_error(kErrTimeout);
   }
+  // the metadata and the NVFP4 factor tables into shared memory
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = static_cast<int>(threadIdx.x) + k * kTqThreads;
+    if (i <= a.G) {
+      sh.ro[i] = m_ro[k];
+      sh.so[i] = m_so[k];
+      if (i < a.G) sh.e[i] = m_e[k];
+    }
+  }
+  if constexpr (FMT == kNVFP4) {
+    if (static_cast<int>(threadIdx.x) < q.n_tab) {
+      float* t = tabs + threadIdx.x * 16;
+      t[0] = 0.0f;
+#pragma unroll
+      for (int m = 1; m < 16; ++m) t[m] = __fdiv_rn(m_sf, static_cast<float>(m));
+    }
+  }
   __syncthreads();
   if (sh.failed != 0u) return;  // block-uniform; reported as BSQ_ERR_TIMEOUT
+  if (gather && reporter) {
+    // source rows outside x: reported when their row belongs to a kept group
+    const uint32_t nb = sh.n_bad;
+    if (nb <= static_cast<uint32_t>(kTqBadList)) {
+      for (uint32_t j = threadIdx.x; j < nb; j += kTqThreads) {
+        int64_t sr;
+        int e;
+        tq_check(a, sh, sh.bad_d[j], sh.bad_src[j], sr, e);
+      }
+    } else {
+      for (int64_t d = threadIdx.x; d < rows; d += kTqThreads) {  // more than the list holds: look again
+        const int32_t src = __ldg(a.row_indices + d);
+        if (src < 0 || src >= a.in_rows) {
+          int64_t sr;
+          int e;
+          tq_check(a, sh, d, src, sr, e);
+        }
+      }
+    }
+  }
 
-  // (2) + (3): warp w takes tokens w, w + 32, ...
   const float* div6 = sh.div6_tab;
+  if (q.units) {
+    // (2) each warp describes tokens w, w + 32 into the freed staging area ...
+    TqDesc* tdesc = reinterpret_cast<TqDesc*>(stage);                   // nt x kTqBucket
+    int* tnv = reinterpret_cast<int*>(tdesc + static_cast<int64_t>(nt) * kTqBucket);  // nt
+#pragma unroll 1
+    for (int k = warp; k < nt; k += kTqWarps) {
+      const int64_t t = t_lo + k;
+      int n;
+      int64_t d = -1;
+      if (gather) {
+        n = static_cast<int>(cnt[k]);
+        if (n > kTqBucket) {  // warp-uniform: left to the re-scan
+          if (lane == 0) {
+            sh.heavy = 1u;
+            tnv[k] = 0;
+          }
+          continue;
+        }
+        if (lane < n) d = bkt[k * kTqBucket + lane];
+      } else {
+        n = t < rows ? 1 : 0;
+        d = t;
+      }
+      const int nv = tq_describe<FMT>(a, sh, tdesc + k * kTqBucket, lane < n, d, t, q.n_tab);
+      if (lane == 0) tnv[k] = nv;
+    }
+    __syncthreads();
+    // (3) ... then claims (token, step) units: the warps of a block share
+    // its tokens' work evenly however few tokens it has.  Unit u is step
+    // u % steps of token u / steps; warp w starts on unit w (prefetched),
+    // and the first step of the next unit is loaded during the last step
+    // of the current one.
+    const int n_units = nt * steps;
+    int u = warp;
+#pragma unroll 1
+    while (u < n_units) {
+      int nxt = 0;
+      if (lane == 0) nxt = static_cast<int>(atomicAdd(&sh.next_unit, 1u));
+      nxt = __shfl_sync(0xFFFFFFFFu, nxt, 0);
+      const int k = u / steps, c = u - k * steps;
+      const int nv = tnv[k];
+      const uint16_t* next_row = nullptr;
+      int next_jb = 0;
+      if (nxt < n_units) {
+        const int nk = nxt / steps;
+        if (t_lo + nk < a.in_rows) {  // (without row_indices, tokens past x have no rows)
+          next_row = a.in + (t_lo + nk) * a.ld_in;
+          next_jb = (nxt - nk * steps) * 32;
+        }
+      }
+      if (nv == 0) {  // warp-uniform: no rows to write; load the next unit's first step
+        tq_zero(pre);
+        if (next_row != nullptr && next_jb + lane < a.K / Fmt<FMT>::SF)
+          tq_load(pre, next_row + Fmt<FMT>::SF * (next_jb + lane), a.in_vec32 != 0);
+      } else {
+        const int jb = c * 32;
+        const int je = min(jb + 32, a.kt_atoms * 4);
+        tq_row<FMT>(a, a.in + (t_lo + k) * a.ld_in, pre, jb, je, tdesc + k * kTqBucket, nv, div6, tabs, next_row,
+                    next_jb);
+      }
+      __syncwarp();
+      u = nxt;
+    }
+  }
+  // (2) + (3) without units: warp w takes tokens w, w + 32, ...
   TqDesc* desc = sh.desc[warp];
 #pragma unroll 1
-  for (int k = warp; k < nt; k += kTqWarps) {
+  for (int k = q.units ? nt : warp; k < nt; k += kTqWarps) {
     const int64_t t = t_lo + k;
     int n;
     int64_t d = -1;
