@@ -4,10 +4,11 @@
 // Persistent: one 1024-thread block per SM, each owning an equal share of
 // the source rows (tokens), so every SM gets the same work when tokens carry
 // the same number of destination rows.  A block
-//   (1) issues each warp's first token-row loads, then scans all of
-//       row_indices itself (16-byte loads; the 128 KB of a 32768-row prefill
-//       stay in L2 for the other blocks) and files every destination row
-//       whose source row it owns into a per-token bucket in shared memory;
+//   (1) issues each warp's first token-row loads and the group metadata
+//       loads (held in registers), then scans all of row_indices itself
+//       (staged by bulk copies; the 128 KB of a 32768-row prefill stay in L2
+//       for the other blocks) and files every destination row whose source
+//       row it owns into a per-token bucket in shared memory;
 //   (2) builds, per token, the list of its destination rows (group, 5D scale
 //       row, expert scale: the same checks as the other grouped kernels);
 //   (3) streams the token row once, 32 lanes on 32 consecutive scale blocks
@@ -15,6 +16,9 @@
 //       to FP32 once, then for every destination row only the per-row scale,
 //       the products and the conversions (MX: the codes do not depend on the
 //       row and are encoded once, then stored per row).
+// Warp w takes tokens w, w + 32, ...; a block with at most kTqUnitTokens
+// tokens (fewer than its warps) instead lets its warps claim (token, step)
+// units from a shared-memory counter, so that every warp works.
 // A token with more destination rows than a bucket holds is left to a
 // re-scan after the others (rare: never with top-k routing to distinct
 // experts); its rows are then quantized one at a time.
