@@ -492,3 +492,66 @@ def test_token_kernel_wide_rows(bsq):
              total_scale_rows=int(so[-1]), G=2)
     p, s = _run_grouped(bsq, "nvfp4", d, 8, kernel="token")
     _compare("nvfp4", d, p, s)
+
+
+@pytest.mark.parametrize("n_bad", [2, 100])
+@pytest.mark.parametrize("skipped", [False, True])
+def test_token_kernel_bad_source_rows_list_and_rescan(bsq, n_bad, skipped):
+    """Source rows outside x seen by the token kernel's scan: a few (kept in
+    its list and checked once the metadata is in shared memory) and 100
+    (more than the list holds: checked by a second pass over row_indices).
+    In a kept group they are reported (BSQ_ERR_VALUE) and their rows left
+    untouched; in a skipped group (negative expert id) nothing is reported.
+    Every other row equals the oracle."""
+    d = wl.config_grouped_prefill(seed=17, tokens=600, K=64, num_experts=8, top_k=2)
+    g = int(np.argmax(np.diff(d["row_offsets"].astype(np.int64))))      # the largest group
+    r0, r1 = int(d["row_offsets"][g]), int(d["row_offsets"][g + 1])
+    assert r1 - r0 >= n_bad
+    rng = np.random.Generator(np.random.PCG64(n_bad))
+    bad = np.sort(rng.choice(np.arange(r0, r1), n_bad, replace=False))
+    ridx = d["row_indices"].copy()
+    ridx[bad] = np.where(np.arange(n_bad) % 2 == 0, -3, 600 + np.arange(n_bad))
+    eid = d["expert_ids"].copy()
+    if skipped:
+        eid[g] = -1
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, ridx=ridx, expert_ids=eid, expect_error=0 if skipped else 4,
+                        kernel="token")
+    safe = np.where((ridx < 0) | (ridx >= 600), 0, ridx)
+    p_ref, pw, s_ref, sw = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"], d["scales_offsets"], eid,
+                                                   d["sf_tensor"], safe)
+    good = pw.copy()
+    good[bad] = False
+    np.testing.assert_array_equal(p[good], p_ref[good])
+    assert np.all(p[bad] == SENTINEL)
+    assert np.all(p[~pw] == SENTINEL)
+    assert bsq.device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+def test_token_kernel_full_buckets_many_tokens_per_block(bsq, fmt):
+    """More than 16 tokens per block (warps take whole tokens rather than
+    shared (token, step) units) with one source row in 40 positions, one in
+    exactly 16 and one in 17, and row_indices 4 bytes past a 16-byte
+    boundary: the re-scan of the static path, against the oracle."""
+    d = wl.config_grouped_prefill(seed=23, tokens=4000, K=32, num_experts=8, top_k=3, fmt=fmt)
+    rng = np.random.Generator(np.random.PCG64(24))
+    ridx = d["row_indices"].copy()
+    ridx[np.isin(ridx, [7, 11, 13])] = 5
+    n = ridx.size
+    pos = rng.permutation(np.arange(3, n - 3))
+    ridx[np.concatenate([[0, 1, 2, n - 3, n - 2, n - 1], pos[:34]])] = 7
+    ridx[pos[34:50]] = 11
+    ridx[pos[50:67]] = 13
+    dev = i32_device(np.concatenate([[0, 0, 0, 0, 7], ridx]))[5:]   # 20 bytes into a 16-byte aligned buffer
+    assert dev.data_ptr() % 16 == 4
+    total_rows, tsr = d["total_rows"], d["total_scale_rows"]
+    ofull, out = guarded(total_rows * oracle.packed_row_bytes(fmt, 32))
+    sfull, sc = guarded(oracle.scales5d_bytes(tsr, 32 // oracle.block_size(fmt)))
+    bsq.grouped_quantize(to_device_bf16(d["x_bits"]), fmt, u32_device(d["row_offsets"]),
+                         u32_device(d["scales_offsets"]), i32_device(d["expert_ids"]),
+                         torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None, dev,
+                         total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=1, out=out, scales=sc,
+                         kernel="token")
+    assert bsq.device_error() == 0
+    assert margin_intact(ofull) and margin_intact(sfull)
+    _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy(), ridx=ridx)
