@@ -95,3 +95,31 @@ def test_fused_epilogue_full_size_persistent_tiles(bsq, fmt):
     mag = np.abs(a64) @ np.abs(b64).T
     err = np.abs(_bf16_to_f64(c_bits[rows]) - c64)
     assert np.all(err <= 2.0 ** -8 * np.abs(c64) + K * 2.0 ** -23 * mag + 1e-30)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("N", [2048, 1920])
+def test_fused_epilogue_partial_round_and_tile_column(bsq, fmt, N):
+    """2560 x N x 256: 160 output tiles of 128 x 256, more than one round of
+    the persistent grid (a partial last round); at N = 1920 the last tile
+    column is half outside C.  Bytes equal the oracle's quantize of the
+    kernel's own BF16 product, which matches FP64 within the FP32
+    accumulation bound."""
+    M, K = 2560, 256
+    rng = np.random.Generator(np.random.PCG64(N + K))
+    a_bits = wl.dense_activations(rng, M, K, "rowlognormal")
+    b_bits = wl.dense_activations(rng, N, K, "normal")
+    a, b = to_device_bf16(a_bits), to_device_bf16(b_bits)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tsf = 3.0 if fmt == "nvfp4" else 1.0
+    out, sc = bsq.gemm_quantize(a, b, fmt, tsf, c_out=c)
+    c_bits = c.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert bsq.device_error() == 0
+    p_ref, s_ref = oracle.quantize(fmt, c_bits, np.float32(tsf))
+    np.testing.assert_array_equal(out.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(sc.cpu().numpy(), s_ref)
+    a64, b64 = _bf16_to_f64(a_bits), _bf16_to_f64(b_bits)
+    c64 = a64 @ b64.T
+    mag = np.abs(a64) @ np.abs(b64).T
+    err = np.abs(_bf16_to_f64(c_bits) - c64)
+    assert np.all(err <= 2.0 ** -8 * np.abs(c64) + K * 2.0 ** -23 * mag + 1e-30)
