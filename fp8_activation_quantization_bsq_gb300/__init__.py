@@ -28,7 +28,7 @@ from ._build import LIB_PATH
 
 __all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes",
            "scales5d_bytes", "quantize", "quantize_dynamic", "tensor_sf", "grouped_tensor_sf",
-           "grouped_quantize", "scales_interleave", "block_scaled_dot", "gemm_quantize", "device_error",
+           "grouped_quantize", "grouped_quantize_workspace_bytes", "scales_interleave", "block_scaled_dot", "gemm_quantize", "device_error",
            "status_string"]
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
@@ -49,6 +49,10 @@ _SIGNATURES = {
     "bsq_grouped_quantize_kernel": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p,
                                              _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64,
                                              _c_p, _c_p, _c_i32, _c_i32, _c_p]),
+    "bsq_grouped_quantize_workspace_bytes": (_c_i64, [_c_i32, _c_i64, _c_i64]),
+    "bsq_grouped_quantize_ws": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p,
+                                         _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i64, _c_i64,
+                                         _c_p, _c_p, _c_i32, _c_i32, _c_p, _c_i64, _c_p]),
     "bsq_scales_interleave": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p]),
     "bsq_quantize_dynamic": (_c_i32, [_c_i32, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p]),
     "bsq_tensor_sf_workspace_bytes": (_c_i64, []),
@@ -217,7 +221,7 @@ def _check_x(x):
 def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_ids,
                      sf_tensor=None, row_indices=None, total_rows: int | None = None,
                      total_scale_rows: int | None = None, k_tiles_per_block: int = 1,
-                     out=None, scales=None, stream=None, kernel: str = "auto"):
+                     out=None, scales=None, stream=None, kernel: str = "auto", workspace=None):
     """Grouped per-expert quantize of the (in_rows, K) BF16 CUDA tensor ``x``.
 
     ``row_offsets`` / ``scales_offsets`` are uint32 (stored as torch.int32
@@ -228,7 +232,10 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
     (groups of many rows), "latency" (groups of a few rows) or "token" (a
     row_indices gather that reuses source rows: each read once); the results
     do not depend on it.  ``k_tiles_per_block``: 1, 2, 4, 8, or 0 (chosen by
-    the library).
+    the library).  ``workspace``: None, or a CUDA uint8 tensor of at least
+    ``grouped_quantize_workspace_bytes(fmt, total_scale_rows, K)`` bytes in
+    which the token kernel stages NVFP4 scale rows (same results; in use
+    until the call's work on the stream completes; MX formats ignore it).
     Returns (packed uint8 (total_rows, packed_row_bytes), scales uint8).
     """
     if kernel not in GROUPED_KERNELS:
@@ -250,13 +257,20 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
         scales = torch.empty(scales5d_bytes(f, total_scale_rows, K), dtype=torch.uint8, device=x.device)
     num_experts = sf_tensor.numel() if sf_tensor is not None else 0
     with torch.cuda.device(x.device):
-        rc = lib().bsq_grouped_quantize_kernel(
+        rc = lib().bsq_grouped_quantize_ws(
             f, _ptr(x), in_rows, K, x.stride(0) if in_rows else K, _ptr(row_offsets),
             _ptr(scales_offsets), _ptr(expert_ids), _ptr(sf_tensor), num_experts,
             _ptr(row_indices), G, total_rows, total_scale_rows, _ptr(out), _ptr(scales),
-            k_tiles_per_block, GROUPED_KERNELS[kernel], _stream(x.device, stream))
+            k_tiles_per_block, GROUPED_KERNELS[kernel], _ptr(workspace),
+            workspace.numel() * workspace.element_size() if workspace is not None else 0,
+            _stream(x.device, stream))
     _check(rc, "bsq_grouped_quantize")
     return out, scales
+
+
+def grouped_quantize_workspace_bytes(fmt, total_scale_rows: int, K: int) -> int:
+    """Bytes of the ``workspace`` of :func:`grouped_quantize`."""
+    return int(lib().bsq_grouped_quantize_workspace_bytes(_fmt(fmt), total_scale_rows, K))
 
 
 def scales_interleave(scales2d: torch.Tensor, out=None, stream=None):

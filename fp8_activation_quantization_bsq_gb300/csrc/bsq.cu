@@ -234,8 +234,19 @@ bsq_status launch_grouped_token(const GroupedArgs& a, cudaStream_t stream) {
              static_cast<size_t>(q.stage_ints) * 8 >= static_cast<size_t>(q.tpb) * (kTqBucket * sizeof(TqDesc) + 4))
                 ? 1 : 0;
   const size_t smem = tq_smem_bytes(q.tpb, q.n_tab, q.stage_ints);
-  const cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)),
-                                   dim3(kTqThreads), smem, stream, a, q);
+  if (a.scale_ws != nullptr && ceil_div(a.kt_atoms, kIlvAtoms) > 65535) return BSQ_ERR_SHAPE;
+  cudaError_t e = launch_pdl(grouped_token_kernel<FMT>, dim3(static_cast<unsigned>(blocks)), dim3(kTqThreads), smem,
+                             stream, a, q);
+  // scale rows staged in the workspace: to their 5D positions
+  if (e == cudaSuccess && a.scale_ws != nullptr) {
+    const dim3 grid(static_cast<unsigned>(a.total_scale_rows / 128),
+                    static_cast<unsigned>(ceil_div(a.kt_atoms, kIlvAtoms)));
+    // 16-byte staging loads when every staged row starts on a 16-byte boundary
+    if (a.kt_atoms % 4 == 0)
+      e = launch_pdl(grouped_scale_ws_kernel<16>, grid, dim3(kIlvThreads), 0, stream, a);
+    else
+      e = launch_pdl(grouped_scale_ws_kernel<4>, grid, dim3(kIlvThreads), 0, stream, a);
+  }
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -270,7 +281,8 @@ bsq_status launch_gemm_quant(const GemmQuantArgs& p, const void* a, int64_t lda,
 }
 
 template <int FMT>
-bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t stream) {
+bsq_status launch_grouped(const GroupedArgs& a_in, int kt, int kernel, cudaStream_t stream) {
+  GroupedArgs a = a_in;
   if (kernel == BSQ_GROUPED_AUTO) {
     if (a.total_rows <= kGroupedLatencyMaxAvgRows * a.G)
       kernel = BSQ_GROUPED_LATENCY;
@@ -287,7 +299,11 @@ bsq_status launch_grouped(const GroupedArgs& a, int kt, int kernel, cudaStream_t
   // the token kernel files destination rows as 32-bit indices
   if (kernel == BSQ_GROUPED_TOKEN && (a.G > kTqMaxGroups || a.total_rows >= (int64_t(1) << 32)))
     kernel = BSQ_GROUPED_STREAM;
+  // the staging pays only for NVFP4 (per-destination scales: 8 atoms per
+  // store of a step); MX and the other kernels store the scales in place
+  if (FMT != kNVFP4) a.scale_ws = nullptr;
   if (kernel == BSQ_GROUPED_TOKEN) return launch_grouped_token<FMT>(a, stream);
+  a.scale_ws = nullptr;
   if (kernel == BSQ_GROUPED_STREAM) return launch_grouped_band<FMT>(a, stream);
   if (kt == 0) {
     // automatic: the fewest atom columns per unit that still keep the grid
@@ -487,6 +503,23 @@ int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows
                                     const int32_t* row_indices, int32_t G, int64_t total_rows,
                                     int64_t total_scale_rows, void* out, void* scales,
                                     int32_t k_tiles_per_block, int32_t kernel, void* stream) {
+  return bsq_grouped_quantize_ws(fmt, in, in_rows, K, ld_in, row_offsets, scales_offsets, expert_ids, sf,
+                                 num_experts, row_indices, G, total_rows, total_scale_rows, out, scales,
+                                 k_tiles_per_block, kernel, nullptr, 0, stream);
+}
+
+int64_t bsq_grouped_quantize_workspace_bytes(int32_t fmt, int64_t total_scale_rows, int64_t K) {
+  if (!fmt_ok(fmt) || total_scale_rows < 0 || K < 0) return 0;
+  // staged scale rows, then one int32 per 128-row band
+  return total_scale_rows * ceil_div(K / sf_of(fmt), 4) * 4 + ceil_div(total_scale_rows / 128 * 4, 16) * 16;
+}
+
+int32_t bsq_grouped_quantize_ws(int32_t fmt, const void* in, int64_t in_rows, int64_t K, int64_t ld_in,
+                                const uint32_t* row_offsets, const uint32_t* scales_offsets,
+                                const int32_t* expert_ids, const float* sf, int32_t num_experts,
+                                const int32_t* row_indices, int32_t G, int64_t total_rows,
+                                int64_t total_scale_rows, void* out, void* scales, int32_t k_tiles_per_block,
+                                int32_t kernel, void* workspace, int64_t workspace_bytes, void* stream) {
   if (!fmt_ok(fmt)) return BSQ_ERR_VALUE;
   if (k_tiles_per_block != 0 && k_tiles_per_block != 1 && k_tiles_per_block != 2 && k_tiles_per_block != 4 &&
       k_tiles_per_block != 8)
@@ -506,10 +539,13 @@ int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in, int64_t in_rows
   if (fmt == BSQ_NVFP4 && num_experts < 1) return BSQ_ERR_VALUE;
   if (!aligned(in, 16) || ld_in % 8 != 0 || !aligned(out, 16) || !aligned(scales, 16) ||
       !aligned(row_offsets, 4) || !aligned(scales_offsets, 4) || !aligned(expert_ids, 4) ||
-      !aligned(sf, 4) || !aligned(row_indices, 4))
+      !aligned(sf, 4) || !aligned(row_indices, 4) || !aligned(workspace, 16))
     return BSQ_ERR_ALIGN;
+  if (workspace != nullptr && workspace_bytes < bsq_grouped_quantize_workspace_bytes(fmt, total_scale_rows, K))
+    return BSQ_ERR_SHAPE;
 
   GroupedArgs a{};
+  a.scale_ws = static_cast<uint8_t*>(workspace);
   a.in = static_cast<const uint16_t*>(in);
   a.ld_in = ld_in;
   a.in_rows = in_rows;

@@ -63,7 +63,38 @@ struct GroupedArgs {
   int in_vec32;         // input rows allow 32-byte loads
   int out_vec32;        // packed rows allow 32-byte stores
   int ktc;              // 32-element chunks per thread block (band kernel)
+  uint8_t* scale_ws;    // token kernel: scale rows staged row-major here (null: straight to 5D),
+                        // then one int32 per 128-row band: its rows written (ws_band_rows)
 };
+
+// Rows of 5D band b (scale rows 128 b ..) that the grouped quantize writes:
+// with g the last group with scales_offsets[g] <= 128 b, the band's rows
+// that are destination rows of g below min(row_offsets[G], total_rows); 0
+// when g is skipped (expert id < 0 or, NVFP4, >= num_experts) or no group
+// starts at or below the band.  ro / so / e: the group metadata (any
+// memory space).
+__device__ __forceinline__ int band_rows_written(const GroupedArgs& a, const uint32_t* ro, const uint32_t* so,
+                                                 const int32_t* e, int64_t b) {
+  const int64_t s0 = b * 128;
+  int lo = 0, hi = a.G;  // g = max{g : so[g] <= s0}
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(so[mid]) <= s0) lo = mid;
+    else hi = mid - 1;
+  }
+  if (lo >= a.G || static_cast<int64_t>(so[lo]) > s0) return 0;
+  const int ex = e[lo];
+  if (ex < 0 || (a.sf != nullptr && ex >= a.num_experts)) return 0;
+  const int64_t ro_end = ro[a.G];
+  const int64_t rows = ro_end < a.total_rows ? ro_end : a.total_rows;
+  const int64_t r_end = ro[lo + 1];
+  const int64_t first = static_cast<int64_t>(ro[lo]) + (s0 - so[lo]);
+  int64_t n = (r_end < rows ? r_end : rows) - first;
+  return static_cast<int>(n < 0 ? 0 : (n > 128 ? 128 : n));
+}
+__device__ __forceinline__ int32_t* ws_band_rows(const GroupedArgs& a) {
+  return reinterpret_cast<int32_t*>(a.scale_ws + a.total_scale_rows * static_cast<int64_t>(a.kt_atoms) * 4);
+}
 
 // Checks of the offsets' first and last entries (one thread reports).
 __device__ __forceinline__ void check_offsets(const GroupedArgs& a) {

@@ -23,12 +23,20 @@
 // re-scan after the others (rare: never with top-k routing to distinct
 // experts); its rows are then quantized one at a time.
 //
+// Scale bytes go to their 5D positions, or, with a caller workspace, to a
+// row-major staging row per 5D scale row (scale_ws): one destination row's
+// 32 scale bytes of a step then fill one 32-byte sector instead of landing
+// in 8 atoms 512 bytes apart (8 partial sectors per store instruction), and
+// grouped_scale_ws_kernel moves the staged rows to the 5D layout afterwards
+// with whole-atom stores, writing only the rows the quantize wrote.
+//
 // NVFP4 element scale tsf / ds without a division: per expert a table of
 // fl32(tsf / m), m = 1..15, and tk_factor's power-of-two step (exact for
 // 2^-117 <= tsf <= 2^118; other scales divide).
 #pragma once
 
 #include "grouped_quant.cuh"
+#include "interleave.cuh"
 
 namespace bsq {
 
@@ -138,8 +146,10 @@ __device__ __forceinline__ int tq_describe(const GroupedArgs& a, TqShared& sh, T
   if (ok) {
     TqDesc dd;
     dd.out = a.out + d * a.out_ld;
-    dd.scale = a.scales + (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512 + (srow & 31) * 16 +
-               ((srow & 127) >> 5) * 4;
+    dd.scale = a.scale_ws != nullptr
+                   ? a.scale_ws + srow * static_cast<int64_t>(a.kt_atoms) * 4  // row-major staging row
+                   : a.scales + (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512 + (srow & 31) * 16 +
+                         ((srow & 127) >> 5) * 4;
     dd.tsf = 1.0f;
     dd.tab = -1;
     if constexpr (FMT == kNVFP4) {
@@ -219,7 +229,7 @@ __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_
       tq_load(nx, next_row + SF * (next_jb + lane), vec32);  // the first step of the warp's next run
     }
     const bool has = j < S, has_scale = j < S4;
-    const int64_t sc_off = static_cast<int64_t>(j >> 2) * 512 + (j & 3);
+    const int64_t sc_off = a.scale_ws != nullptr ? static_cast<int64_t>(j) : static_cast<int64_t>(j >> 2) * 512 + (j & 3);
     uint32_t acc = 0;
 #pragma unroll
     for (int c = 0; c < SF / 8; ++c) {
@@ -499,6 +509,12 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
   }
   __syncthreads();
   if (sh.failed != 0u) return;  // block-uniform; reported as BSQ_ERR_TIMEOUT
+  if (a.scale_ws != nullptr) {  // the staged rows of each band, for grouped_scale_ws_kernel
+    const int64_t n_bands = a.total_scale_rows / 128;
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * kTqThreads + threadIdx.x; b < n_bands;
+         b += static_cast<int64_t>(gridDim.x) * kTqThreads)
+      ws_band_rows(a)[b] = band_rows_written(a, sh.ro, sh.so, sh.e, b);
+  }
   if (gather && reporter) {
     // source rows outside x: reported when their row belongs to a kept group
     const uint32_t nb = sh.n_bad;
@@ -641,6 +657,60 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
         tq_load(c, a.in + static_cast<int64_t>(ss) * a.ld_in + Fmt<FMT>::SF * lane, a.in_vec32 != 0);
       tq_row<FMT>(a, a.in + static_cast<int64_t>(ss) * a.ld_in, c, 0, a.kt_atoms * 4, desc, nv, div6, tabs);
       __syncwarp();
+    }
+  }
+}
+
+// ------------------------------------------------- grouped_scale_ws_kernel --
+
+// Block (b, c): 5D band b (scale rows 128 b ..), atoms kIlvAtoms c ..  The
+// token kernel stored n = band_rows_written(b) in the workspace after the
+// staged rows; those n rows (row-major, 4 Kt bytes each) go to their 5D
+// positions: a 16-byte store per chunk whose four rows were all written,
+// 4-byte stores otherwise; the other rows' bytes are not touched.  VEC:
+// bytes per staging load (16 when the rows allow it, else 4).
+template <int VEC>
+__global__ void __launch_bounds__(kIlvThreads) grouped_scale_ws_kernel(const GroupedArgs a) {
+  __shared__ __align__(16) uint8_t tile[128 * kIlvPitch];
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * 128;
+  pdl_wait();
+  const int n = __ldcg(ws_band_rows(a) + blockIdx.x);  // written by the token kernel
+  if (n <= 0 || n > 128) return;  // block-uniform
+
+  const int kt = a.kt_atoms;
+  const int a0 = blockIdx.y * kIlvAtoms;
+  const int na = min(kIlvAtoms, kt - a0);
+  const int64_t S4 = static_cast<int64_t>(kt) * 4;
+  const uint8_t* src = a.scale_ws + s0 * S4 + 4 * a0;  // staged row r, this run's first byte
+  // rows r < n, bytes 0 .. 4 na - 1 of the run, into the padded tile
+  constexpr int kPerRow = kIlvCols / VEC;
+  for (int idx = threadIdx.x; idx < 128 * kPerRow; idx += kIlvThreads) {
+    const int r = idx / kPerRow, w = idx % kPerRow;
+    if (r < n && VEC * w < 4 * na) {
+      if constexpr (VEC == 16) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + r * S4 + VEC * w));
+        uint32_t* t = reinterpret_cast<uint32_t*>(tile + r * kIlvPitch + VEC * w);
+        t[0] = x.x; t[1] = x.y; t[2] = x.z; t[3] = x.w;
+      } else {
+        *reinterpret_cast<uint32_t*>(tile + r * kIlvPitch + VEC * w) =
+            __ldg(reinterpret_cast<const uint32_t*>(src + r * S4 + VEC * w));
+      }
+    }
+  }
+  __syncthreads();
+  uint8_t* dst = a.scales + (static_cast<int64_t>(blockIdx.x) * kt + a0) * 512;
+  for (int idx = threadIdx.x; idx < na * 32; idx += kIlvThreads) {
+    const int at = idx >> 5, r32 = idx & 31;
+    if (r32 >= n) continue;
+    const uint8_t* t = tile + r32 * kIlvPitch + at * 4;
+    uint8_t* chunk = dst + at * 512 + r32 * 16;
+    if (r32 + 96 < n) {
+      st_global_v4(chunk, *reinterpret_cast<const uint32_t*>(t), *reinterpret_cast<const uint32_t*>(t + 32 * kIlvPitch),
+                   *reinterpret_cast<const uint32_t*>(t + 64 * kIlvPitch),
+                   *reinterpret_cast<const uint32_t*>(t + 96 * kIlvPitch));
+    } else {
+      for (int sb = 0; sb < 4 && r32 + 32 * sb < n; ++sb)
+        *reinterpret_cast<uint32_t*>(chunk + 4 * sb) = *reinterpret_cast<const uint32_t*>(t + 32 * sb * kIlvPitch);
     }
   }
 }

@@ -195,6 +195,49 @@ BSQ_API int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in_dev, int
                                             int32_t kernel, void* stream);
 
 /*
+ * Workspace bytes of bsq_grouped_quantize_ws: total_scale_rows * ceil(S/4) * 4
+ * (one row-major scale row per 5D scale row, the size of the 5D scale
+ * buffer) plus 4 bytes per 128-row band, rounded up to 16; 0 for bad
+ * arguments.
+ */
+BSQ_API int64_t bsq_grouped_quantize_workspace_bytes(int32_t fmt, int64_t total_scale_rows, int64_t K);
+
+/*
+ * bsq_grouped_quantize_kernel with a caller workspace for the token kernel's
+ * NVFP4 scales.  The token kernel (BSQ_GROUPED_TOKEN, or AUTO choosing it)
+ * then writes each destination row's scale bytes row-major into the
+ * workspace (whole sectors instead of 4 bytes in each of 8 atoms) and a
+ * second kernel moves the rows it wrote to their 5D positions with
+ * whole-atom stores.  MX formats and the other kernels ignore the
+ * workspace.  It pays off when the scale stores dominate (many destination
+ * rows per token and long rows, e.g. top-8 routing at K = 7168); with few
+ * destination rows per token the second launch costs more than it saves.
+ * The bytes of out_dev and scales5d_dev are identical to
+ * bsq_grouped_quantize_kernel's (padding scale rows and the rows of skipped
+ * groups are not written); on a reported device error the scale bytes of
+ * the offending rows are unspecified.
+ *
+ *   workspace_dev    NULL (then exactly bsq_grouped_quantize_kernel), or
+ *                    device memory of at least
+ *                    bsq_grouped_quantize_workspace_bytes(fmt, total_scale_rows, K)
+ *                    bytes, 16-byte aligned, overlapping no other argument.
+ *                    Its contents need no initialisation and are unspecified
+ *                    afterwards; it is in use until the call's work on
+ *                    `stream` completes (reuse it in stream order).
+ *   workspace_bytes  its size.
+ * Errors: BSQ_ERR_ALIGN for a misaligned workspace, BSQ_ERR_SHAPE for a
+ * smaller one; otherwise as bsq_grouped_quantize_kernel.
+ */
+BSQ_API int32_t bsq_grouped_quantize_ws(int32_t fmt, const void* in_dev, int64_t in_rows, int64_t K,
+                                        int64_t ld_in, const uint32_t* row_offsets_dev,
+                                        const uint32_t* scales_offsets_dev, const int32_t* expert_ids_dev,
+                                        const float* sf_dev, int32_t num_experts,
+                                        const int32_t* row_indices_dev, int32_t G, int64_t total_rows,
+                                        int64_t total_scale_rows, void* out_dev, void* scales5d_dev,
+                                        int32_t k_tiles_per_block, int32_t kernel, void* workspace_dev,
+                                        int64_t workspace_bytes, void* stream);
+
+/*
  * Rank-2 -> 5D scale reinterleave (block_scales_interleave / _fp4 / _fp4_kernel).
  *
  *   scales2d_dev  M rows of S scale bytes, row stride ld bytes (ld >= S).

@@ -248,3 +248,35 @@ def test_gemm_quantize_validation(lib):
     assert call(fmt=0, tsf=float("inf")) == VALUE
     assert call(M=0, a=None, b=None, out=None, sc=None) == OK   # empty: no-op
 
+
+
+def test_grouped_workspace_validation(lib):
+    """bsq_grouped_quantize_ws: the workspace size helper, a misaligned
+    workspace (BSQ_ERR_ALIGN), a short one (BSQ_ERR_SHAPE), and a NULL one
+    (the call goes on to its other checks)."""
+    lib.bsq_grouped_quantize_workspace_bytes.restype = ctypes.c_int64
+    lib.bsq_grouped_quantize_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
+    lib.bsq_scales5d_bytes.restype = ctypes.c_int64
+    lib.bsq_scales5d_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
+    for fmt in (0, 1, 2):
+        for rows, K in ((512, 256), (128, 96), (0, 64), (384, 7168)):
+            bands = rows // 128
+            assert lib.bsq_grouped_quantize_workspace_bytes(fmt, rows, K) == \
+                lib.bsq_scales5d_bytes(fmt, rows, K) + -(-bands * 4 // 16) * 16
+    assert lib.bsq_grouped_quantize_workspace_bytes(3, 128, 64) == 0
+    assert lib.bsq_grouped_quantize_workspace_bytes(0, -1, 64) == 0
+    f = lib.bsq_grouped_quantize_ws
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p]
+    need = lib.bsq_grouped_quantize_workspace_bytes(0, 512, 256)
+
+    def call(ws, ws_bytes, out=P):
+        return f(0, P, 64, 256, 256, P, P, P, P, 8, None, 4, 64, 512, out, P, 1, 3, ws, ws_bytes, None)
+    assert call(P + 4, need) == ALIGN
+    assert call(P, need - 1) == SHAPE
+    assert call(None, 0, out=None) == NULL
+    assert call(P, need, out=None) == NULL

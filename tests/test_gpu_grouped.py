@@ -30,7 +30,7 @@ def bsq():
 
 
 def _run_grouped(bsq, fmt, d, kt, use_ridx=True, expert_ids=None, x_bits=None, ridx=None,
-                 expect_error=0, kernel="auto"):
+                 expect_error=0, kernel="auto", workspace=False):
     x_bits = d["x_bits"] if x_bits is None else x_bits
     K = x_bits.shape[1]
     eid = d["expert_ids"] if expert_ids is None else expert_ids
@@ -40,12 +40,18 @@ def _run_grouped(bsq, fmt, d, kt, use_ridx=True, expert_ids=None, x_bits=None, r
     sb = oracle.scales5d_bytes(tsr, K // oracle.block_size(fmt))
     ofull, out = guarded(ob)
     sfull, sc = guarded(sb)
+    ws = None
+    if workspace:  # staged scale rows; its prior contents must not matter
+        wfull, ws = guarded(bsq.grouped_quantize_workspace_bytes(fmt, tsr, K))
+        ws.fill_(0xA5)
     bsq.grouped_quantize(to_device_bf16(x_bits), fmt, u32_device(d["row_offsets"]),
                          u32_device(d["scales_offsets"]), i32_device(eid),
                          torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
                          i32_device(ridx) if ridx is not None else None,
                          total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=kt,
-                         out=out, scales=sc, kernel=kernel)
+                         out=out, scales=sc, kernel=kernel, workspace=ws)
+    if workspace:
+        assert margin_intact(wfull)
     assert bsq.device_error() == expect_error
     assert margin_intact(ofull) and margin_intact(sfull)
     return out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy()
@@ -186,13 +192,14 @@ def _prefill_reference(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8", "mxfp4"])
-@pytest.mark.parametrize("kernel", ["auto", "token", "stream"])
+@pytest.mark.parametrize("kernel", ["auto", "token", "stream", "token+workspace", "auto+workspace"])
 def test_grouped_prefill_full_config_all_rows(bsq, fmt, kernel):
     """Prefill at full size (32768 rows, K = 7168) in the benchmark's launch
-    configuration: every packed row and every written scale byte against the
-    oracle, and the padding scale rows (never written) keep their sentinel."""
+    configuration (also with the scale-staging workspace): every packed row
+    and every written scale byte against the oracle, and the padding scale
+    rows (never written) keep their sentinel."""
     d, (chunks, refs) = _prefill_reference(fmt)
-    p, s = _run_grouped(bsq, fmt, d, 8, kernel=kernel)
+    p, s = _run_grouped(bsq, fmt, d, 8, kernel=kernel.split("+")[0], workspace=kernel.endswith("+workspace"))
     K = d["K"]
     S = K // oracle.block_size(fmt)
     Kt = -(-S // 4)
@@ -449,14 +456,16 @@ def test_token_kernel_shapes(bsq, fmt, tokens, K, top_k, experts):
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
 @pytest.mark.parametrize("K", [96, 2112, 7168])
 @pytest.mark.parametrize("gather", [True, False])
-def test_token_kernel_band_shapes(bsq, fmt, K, gather):
+@pytest.mark.parametrize("ws", [False, True])
+def test_token_kernel_band_shapes(bsq, fmt, K, gather, ws):
     """The token kernel on scale bands of every fill: groups of 128, 127,
     129, 256 and 1 rows (whole, partly filled and single-row bands), an empty
     group, a skipped group that spans whole bands, and a group with a
     reserved, unused padding tile; with and without the row_indices gather.
     Every written byte equals the oracle and every padding scale row keeps
     its sentinel.  K = 96 / 2112 / 7168 give 1, 33 and 112 (NVFP4) atoms per
-    band row."""
+    band row.  With the workspace, the staged scale rows reach exactly the
+    same 5D bytes and nothing else."""
     rng = np.random.Generator(np.random.PCG64(K + 7 * gather))
     m = np.array([128, 0, 127, 129, 256, 300, 128, 1], np.int64)
     tiles = -(-m // 128)
@@ -472,7 +481,7 @@ def test_token_kernel_band_shapes(bsq, fmt, K, gather):
     sf = (rng.random(7).astype(np.float32) + np.float32(0.5)) * np.float32(100.0)
     d = dict(x_bits=x, row_offsets=ro, scales_offsets=so, expert_ids=eid, sf_tensor=sf,
              row_indices=ridx, total_rows=total_rows, total_scale_rows=int(so[-1]), G=G)
-    p, s = _run_grouped(bsq, fmt, d, 8, use_ridx=gather, kernel="token")
+    p, s = _run_grouped(bsq, fmt, d, 8, use_ridx=gather, kernel="token", workspace=ws)
     _compare(fmt, d, p, s, use_ridx=gather)
 
 
@@ -555,3 +564,34 @@ def test_token_kernel_full_buckets_many_tokens_per_block(bsq, fmt):
     assert bsq.device_error() == 0
     assert margin_intact(ofull) and margin_intact(sfull)
     _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy(), ridx=ridx)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("kernel", ["stream", "latency", "token", "auto"])
+@pytest.mark.parametrize("tokens", [67, 4000])
+def test_grouped_workspace_every_kernel(bsq, fmt, kernel, tokens):
+    """The scale-staging workspace with every kernel choice (the streaming
+    and latency kernels ignore it) on top-3 routing with 67 tokens (the
+    token kernel's (token, step) units) and 4000 tokens (whole tokens per
+    warp): bytes equal the oracle, padding rows keep their sentinel."""
+    d = wl.config_grouped_prefill(seed=31 + tokens, tokens=tokens, K=192, num_experts=12, top_k=3, fmt=fmt)
+    p, s = _run_grouped(bsq, fmt, d, 4, kernel=kernel, workspace=True)
+    _compare(fmt, d, p, s)
+
+
+def test_grouped_workspace_bad_source_rows_reported(bsq):
+    """With the workspace, a source row outside x in a kept group is still
+    reported (BSQ_ERR_VALUE) and its packed row left untouched; every other
+    row equals the oracle."""
+    d = wl.config_grouped_prefill(seed=8, tokens=40, K=128, num_experts=8, top_k=2)
+    ridx = d["row_indices"].copy()
+    bad = [3, len(ridx) - 1]
+    ridx[bad[0]] = 10_000_000
+    ridx[bad[1]] = -5
+    p, s = _run_grouped(bsq, "nvfp4", d, 1, ridx=ridx, expect_error=4, kernel="token", workspace=True)
+    p_ref, pw, _, _ = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"], d["scales_offsets"],
+                                              d["expert_ids"], d["sf_tensor"], np.where(ridx < 0, 0, np.minimum(ridx, 39)))
+    good = np.ones(d["total_rows"], bool)
+    good[bad] = False
+    np.testing.assert_array_equal(p[good], p_ref[good])
+    assert np.all(p[bad] == SENTINEL)
