@@ -348,9 +348,10 @@ def extra_workloads(bsq, device, flush, peak):
         del outs, fns
     del xs, x0
 
-    def grouped_sets(d, fmt, kt, sets):
+    def grouped_sets(d, fmt, kt, sets, workspace=False):
         """Launch closures over `sets` buffer sets (token-matrix copy, packed
-        output, 5D scales; the metadata shared) and the algorithmic bytes."""
+        output, 5D scales, optionally the scale-staging workspace; the
+        metadata shared) and the algorithmic bytes."""
         x0 = to_dev_bf16(d["x_bits"], device)
         xgs = [x0] + [x0.clone() for _ in range(sets - 1)]
         u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
@@ -362,8 +363,10 @@ def extra_workloads(bsq, device, flush, peak):
         fns = []
         for xg in xgs:
             out, sc = bsq.grouped_quantize(xg, fmt, ro, so, eid, sf, ridx, **kw)
-            fns.append(lambda xg=xg, out=out, sc=sc: bsq.grouped_quantize(xg, fmt, ro, so, eid, sf, ridx, out=out,
-                                                                          scales=sc, **kw))
+            ws = torch.empty(bsq.grouped_quantize_workspace_bytes(fmt, d["total_scale_rows"], d["K"]),
+                             dtype=torch.uint8, device=device) if workspace else None
+            fns.append(lambda xg=xg, out=out, sc=sc, ws=ws: bsq.grouped_quantize(
+                xg, fmt, ro, so, eid, sf, ridx, out=out, scales=sc, workspace=ws, **kw))
         K = d["K"]
         sfv = 16 if fmt == "nvfp4" else 32
         kt_cols = -(-(K // sfv) // 4) * 4
@@ -405,11 +408,11 @@ def extra_workloads(bsq, device, flush, peak):
     res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(rot * 1e3, 2),
                                                              "us_single_cold": round(single * 1e3, 2)}
     del gouts, so_d, xgs, x0, gsfs, gws, fns
-    for fmt in ("nvfp4", "mxfp8", "mxfp4"):
-        fns, b = grouped_sets(d, fmt, 8, ROT_SETS)
+    for fmt, ws in (("nvfp4", False), ("nvfp4", True), ("mxfp8", False), ("mxfp4", False)):
+        fns, b = grouped_sets(d, fmt, 8, ROT_SETS, workspace=ws)
         rot = time_rotated(fns)
         single, _ = time_events(fns[0], reps, flush)
-        res[f"{fmt}_grouped_prefill_T4096_K7168"] = {
+        res[f"{fmt}_grouped_prefill_T4096_K7168" + ("_workspace" if ws else "")] = {
             "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
             "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
             "algorithmic_bytes": b, "logical_input_bytes": d["total_rows"] * d["K"] * 2,
@@ -703,6 +706,10 @@ def run_case(args):
                                                out=out, workspace=ws)
         else:
             kw["kernel"] = args.grouped_kernel
+            if args.grouped_workspace:
+                kw["workspace"] = torch.empty(bsq.grouped_quantize_workspace_bytes(args.fmt, d["total_scale_rows"],
+                                                                                   d["K"]),
+                                              dtype=torch.uint8, device=device)
             out, sc = bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, **kw)
             fn = lambda: bsq.grouped_quantize(x, args.fmt, ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
     elif args.case == "gemm_quantize":
@@ -760,6 +767,8 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the context workloads")
     ap.add_argument("--grouped-kernel", choices=("auto", "stream", "latency", "token"), default="auto",
                     help="kernel of the grouped --case workloads")
+    ap.add_argument("--grouped-workspace", action="store_true",
+                    help="with --case grouped_*: pass the scale-staging workspace")
     ap.add_argument("--fmt", choices=("nvfp4", "mxfp4", "mxfp8"), default="nvfp4",
                     help="format of the grouped --case workloads")
     ap.add_argument("--case", choices=CASES, default=None,
