@@ -218,7 +218,7 @@ def test_grouped_prefill_full_config_all_rows(bsq, fmt, kernel):
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
-@pytest.mark.parametrize("kernel", ["token", "stream", "latency"])
+@pytest.mark.parametrize("kernel", ["token", "stream", "latency", "token+workspace"])
 def test_grouped_source_row_past_a_full_bucket_offset_indices(bsq, fmt, kernel):
     """row_indices starting 4 bytes past a 16-byte boundary (a scalar head of
     three entries), a row count that is not a multiple of 4 (a scalar tail),
@@ -246,10 +246,13 @@ def test_grouped_source_row_past_a_full_bucket_offset_indices(bsq, fmt, kernel):
     sb = oracle.scales5d_bytes(tsr, 256 // oracle.block_size(fmt))
     ofull, out = guarded(ob)
     sfull, sc = guarded(sb)
+    ws = None
+    if kernel.endswith("+workspace"):
+        ws = torch.full((bsq.grouped_quantize_workspace_bytes(fmt, tsr, 256),), 0x3C, dtype=torch.uint8, device="cuda")
     bsq.grouped_quantize(to_device_bf16(x_bits), fmt, u32_device(d["row_offsets"]), u32_device(d["scales_offsets"]),
                          i32_device(d["expert_ids"]), torch.from_numpy(d["sf_tensor"]).cuda() if fmt == "nvfp4" else None,
                          dev, total_rows=total_rows, total_scale_rows=tsr, k_tiles_per_block=2, out=out, scales=sc,
-                         kernel=kernel)
+                         kernel=kernel.split("+")[0], workspace=ws)
     assert bsq.device_error() == 0
     assert margin_intact(ofull) and margin_intact(sfull)
     _compare(fmt, d, out.cpu().numpy().reshape(total_rows, -1), sc.cpu().numpy(), ridx=ridx)
@@ -421,10 +424,12 @@ def test_grouped_nvfp4_extreme_tensor_scales(bsq, kernel):
 
 
 @pytest.mark.parametrize("G", [1024, 1025])
-def test_grouped_token_kernel_group_limit(bsq, G):
+@pytest.mark.parametrize("ws", [False, True])
+def test_grouped_token_kernel_group_limit(bsq, G, ws):
     """The token kernel keeps the group metadata of up to 1024 groups in
-    shared memory; at 1025 the explicit choice falls back to the band kernel.
-    One- to three-row groups gathered from 900 tokens (rows reused)."""
+    shared memory; at 1025 the explicit choice falls back to the band kernel
+    (which ignores a workspace).  One- to three-row groups gathered from 900
+    tokens (rows reused), with and without the scale-staging workspace."""
     rng = np.random.Generator(np.random.PCG64(G))
     m = rng.integers(1, 4, size=G)
     ro = np.concatenate([[0], np.cumsum(m)]).astype(np.uint32)
@@ -436,7 +441,7 @@ def test_grouped_token_kernel_group_limit(bsq, G):
              row_indices=rng.integers(0, 900, size=rows).astype(np.int32),
              total_rows=rows, total_scale_rows=int(so[-1]), G=G)
     for fmt in ("nvfp4", "mxfp4"):
-        p, s = _run_grouped(bsq, fmt, d, 1, kernel="token")
+        p, s = _run_grouped(bsq, fmt, d, 1, kernel="token", workspace=ws)
         _compare(fmt, d, p, s)
 
 
