@@ -407,6 +407,17 @@ def extra_workloads(bsq, device, flush, peak):
     single, _ = time_events(lambda: gchain(0), reps, flush)
     res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(rot * 1e3, 2),
                                                              "us_single_cold": round(single * 1e3, 2)}
+    # the same chain with the quantize's scale-staging workspace
+    gwss = [torch.empty(bsq.grouped_quantize_workspace_bytes("nvfp4", d["total_scale_rows"], d["K"]),
+                        dtype=torch.uint8, device=device) for _ in range(ROT_SETS)]
+
+    def gchain_ws(i):
+        bsq.grouped_tensor_sf(xgs[i], ro, eid, E, ridx, total_rows=d["total_rows"], out=gsfs[i], workspace=gws)
+        bsq.grouped_quantize(xgs[i], "nvfp4", ro, so_d, eid, gsfs[i], ridx, out=gouts[i][0], scales=gouts[i][1],
+                             workspace=gwss[i], **gkw)
+    rot = time_rotated([lambda i=i: gchain_ws(i) for i in range(ROT_SETS)])
+    res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168_workspace"] = {"us": round(rot * 1e3, 2)}
+    del gwss
     del gouts, so_d, xgs, x0, gsfs, gws, fns
     for fmt, ws in (("nvfp4", False), ("nvfp4", True), ("mxfp8", False), ("mxfp4", False)):
         fns, b = grouped_sets(d, fmt, 8, ROT_SETS, workspace=ws)
