@@ -1,7 +1,8 @@
 """The entry points can be captured into a CUDA graph and replayed: dense
-quantize + scale reinterleave, and the device-side chain tensor_sf ->
+quantize + scale reinterleave, the device-side chain tensor_sf ->
 quantize_dynamic (its workspace leaves itself zeroed, so replays need no
-memset).  Each replay runs on new input copied into the captured buffers
+memset), and the grouped token kernel with and without its scale-staging
+workspace.  Each replay runs on new input copied into the captured buffers
 and must match the oracle bit for bit.  Per-device set-up happens on a
 first call made before the capture."""
 import numpy as np
@@ -88,4 +89,40 @@ def test_graph_tensor_scale_chain(bsq):
         assert got[0] == amax and got[1] == tsf
         np.testing.assert_array_equal(out.cpu().numpy(), p_ref)
         np.testing.assert_array_equal(sc.cpu().numpy(), s_ref)
+    assert bsq.device_error() == 0
+
+
+@pytest.mark.parametrize("ws", [False, True])
+def test_graph_grouped_token_quantize(bsq, ws):
+    """The grouped quantize through the token kernel (and, with the
+    scale-staging workspace, its second kernel) captured once and replayed
+    on new token rows: packed rows and written scale bytes equal the
+    oracle on every replay."""
+    d = wl.config_grouped_prefill(seed=61, tokens=300, K=256, num_experts=16, top_k=4)
+    u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).cuda()
+    ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
+    eid = torch.from_numpy(d["expert_ids"]).cuda()
+    sf = torch.from_numpy(d["sf_tensor"]).cuda()
+    ridx = torch.from_numpy(d["row_indices"]).cuda()
+    x = torch.empty((300, 256), dtype=torch.bfloat16, device="cuda")
+    tsr = d["total_scale_rows"]
+    w = torch.empty(bsq.grouped_quantize_workspace_bytes("nvfp4", tsr, 256), dtype=torch.uint8,
+                    device="cuda") if ws else None
+    kw = dict(total_rows=d["total_rows"], total_scale_rows=tsr, k_tiles_per_block=1, kernel="token", workspace=w)
+    out, sc = bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, **kw)   # set-up before capture
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
+    for seed in (1, 2):
+        rng = np.random.Generator(np.random.PCG64(70 + seed))
+        bits = wl.dense_activations(rng, 300, 256, "blocklognormal")
+        _bits_to_dev(bits, x)
+        p_ref, pw, s_ref, sw = oracle.grouped_quantize("nvfp4", bits, d["row_offsets"], d["scales_offsets"],
+                                                       d["expert_ids"], d["sf_tensor"], d["row_indices"])
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
+        np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
     assert bsq.device_error() == 0
