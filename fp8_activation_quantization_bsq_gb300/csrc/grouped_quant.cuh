@@ -22,7 +22,8 @@
 //  * grouped_rows_kernel (groups of a few rows, decode).  A warp owns R
 //    consecutive destination rows and one run of k_tiles_per_block atom
 //    columns, whatever the group sizes.  Lane r resolves row d0 + r by a
-//    binary search over row_offsets (L1-resident), then the rows' scale
+//    binary search over row_offsets (the group tables staged in shared
+//    memory by one coalesced pass when G <= 1024), then the rows' scale
 //    blocks are spread over the lanes, consecutive blocks on consecutive
 //    lanes, each lane quantizing whole blocks; the scale bytes of a row's
 //    atom are OR-reduced over 4 lanes into one word.
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(32 * band_warps<FMT>()) grouped_band_kernel(co
 
 constexpr int kGrWarps = 4;
 constexpr int kGrThreads = 32 * kGrWarps;
+constexpr int kGrStageGroups = 1024;  // group tables staged in shared memory up to this many groups / experts
 
 // Per-row state of a warp's rows, in shared memory so that any lane can read
 // the row of the block it holds.
@@ -391,39 +393,63 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
 
   __shared__ RowState rs_all[kGrWarps][R];
   __shared__ float div6_tab[128];
+  __shared__ uint32_t ro_s[kGrStageGroups + 1], so_s[kGrStageGroups + 1];
+  __shared__ int32_t e_s[kGrStageGroups];
+  __shared__ float sf_s[kGrStageGroups];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if constexpr (FMT == kNVFP4) fill_div6_table(div6_tab, threadIdx.x, kGrThreads);
-  __syncthreads();
   pdl_wait();
 
-  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kGrWarps + warp) * R;
-  if (d0 >= a.total_rows) return;
+  const int64_t d0_blk = static_cast<int64_t>(blockIdx.x) * kGrWarps * R;
+  if (d0_blk >= a.total_rows) return;  // block-uniform
+  const int64_t d0 = d0_blk + static_cast<int64_t>(warp) * R;
   RowState* rs = rs_all[warp];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_offsets(a);
+  // the row's source index does not depend on its group: in flight first
+  const int64_t dl = d0 + lane;
+  const int64_t src_pre =
+      (lane < R && dl < a.total_rows && a.row_indices) ? static_cast<int64_t>(__ldg(a.row_indices + dl)) : dl;
+  // the group tables in shared memory (one coalesced pass) when they fit, so
+  // that resolving a row costs no chain of dependent global loads
+  const bool staged = a.G <= kGrStageGroups && (a.sf == nullptr || a.num_experts <= kGrStageGroups);
+  if (staged) {
+    for (int i = threadIdx.x; i <= a.G; i += kGrThreads) {
+      ro_s[i] = __ldg(a.row_offsets + i);
+      so_s[i] = __ldg(a.scales_offsets + i);
+      if (i < a.G) e_s[i] = __ldg(a.expert_ids + i);
+    }
+    if (a.sf != nullptr)
+      for (int i = threadIdx.x; i < a.num_experts; i += kGrThreads) sf_s[i] = __ldg(a.sf + i);
+  }
+  __syncthreads();
+  if (d0 >= a.total_rows) return;
 
   // ---- lane r resolves row d0 + r
   if (lane < R) {
-    const int64_t d = d0 + lane;
+    const int64_t d = dl;
     RowState st{d, d, 0, 0, 0, 1.0f};
-    const int64_t ro_end = d < a.total_rows ? static_cast<int64_t>(__ldg(a.row_offsets + a.G)) : 0;
+    const int64_t ro_end =
+        d < a.total_rows ? static_cast<int64_t>(staged ? ro_s[a.G] : __ldg(a.row_offsets + a.G)) : 0;
     if (d < ro_end) {
       // g = max{g : ro[g] <= d}: binary search for the first ro[g+1] > d
       int lo = 0, hi = a.G - 1;
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (static_cast<int64_t>(__ldg(a.row_offsets + mid + 1)) <= d) lo = mid + 1;
+        if (static_cast<int64_t>(staged ? ro_s[mid + 1] : __ldg(a.row_offsets + mid + 1)) <= d) lo = mid + 1;
         else hi = mid;
       }
-      const int64_t r_beg = __ldg(a.row_offsets + lo), r_end = __ldg(a.row_offsets + lo + 1);
-      const int64_t so_g = __ldg(a.scales_offsets + lo), so_n = __ldg(a.scales_offsets + lo + 1);
-      const int e = __ldg(a.expert_ids + lo);
+      const int64_t r_beg = staged ? ro_s[lo] : __ldg(a.row_offsets + lo);
+      const int64_t r_end = staged ? ro_s[lo + 1] : __ldg(a.row_offsets + lo + 1);
+      const int64_t so_g = staged ? so_s[lo] : __ldg(a.scales_offsets + lo);
+      const int64_t so_n = staged ? so_s[lo + 1] : __ldg(a.scales_offsets + lo + 1);
+      const int e = staged ? e_s[lo] : __ldg(a.expert_ids + lo);
       const int64_t srow = so_g + (d - r_beg);
       if (r_end - r_beg < 0 || r_end - r_beg > so_n - so_g || r_end > a.total_rows ||
           srow >= a.total_scale_rows || d < r_beg || (a.sf != nullptr && e >= a.num_experts)) {
         record_error(kErrValue);
       } else if (e >= 0) {
-        const int64_t src = a.row_indices ? static_cast<int64_t>(__ldg(a.row_indices + d)) : d;
+        const int64_t src = src_pre;
         if (src < 0 || src >= a.in_rows) {
           record_error(kErrValue);
         } else {
@@ -431,7 +457,7 @@ __global__ void __launch_bounds__(kGrThreads) grouped_rows_kernel(const GroupedA
           st.band = (srow >> 7) * static_cast<int64_t>(a.kt_atoms) * 512;
           st.atom_off = static_cast<int>((srow & 31) * 16 + ((srow & 127) >> 5) * 4);
           st.ok = 1;
-          if (a.sf != nullptr) st.tsf = __ldg(a.sf + e);
+          if (a.sf != nullptr) st.tsf = staged ? sf_s[e] : __ldg(a.sf + e);
         }
       }
     }
