@@ -5,10 +5,10 @@
 //
 // Dense: warps stride over rows, lanes over 16-byte chunks (four loads in
 // flight per lane), max.xorsign.abs BF16 pairs, warp and block reductions;
-// every block stores its partial max in the workspace, and the last block to
-// finish (fenced atomic counter) reduces the partials and writes
-// {amax, tensor_sf}.  Grouped: one warp per destination row, its group by a
-// binary search over row_offsets, an atomic max per expert (non-negative FP32
+// every block folds its maximum into the workspace with one atomic max, and
+// the last block to finish (fenced atomic counter) writes {amax, tensor_sf}.
+// Grouped: one warp per destination row, its group by a binary search over
+// row_offsets, an atomic max per expert (non-negative FP32
 // maxima order like their bit patterns), and the last block writes sf_tensor;
 // when a gather reuses source rows over few tokens, a token-major variant
 // reads each source row once and scans row_indices instead.  All leave their
@@ -24,19 +24,23 @@ constexpr int kAmaxThreads = 256;
 constexpr int kAmaxWarps = kAmaxThreads / 32;
 constexpr int kAmaxMaxBlocks = 1024;
 
-// Dense workspace: a completion counter and one partial per block.  The
-// caller zeroes it once; the last block of every launch sets the counter
-// back to zero, so consecutive launches need no memset in between.  A stale
-// counter c > 0 (a workspace never zeroed) hands some block a ticket >=
-// gridDim.x, which records BSQ_ERR_VALUE; with c >= gridDim.x no block is
-// last and nothing is written, with a smaller c the block holding ticket
-// gridDim.x - 1 may reduce before the remaining blocks have stored their
-// partials (that launch's outputs are reported as invalid).  Each launch
-// writes every partial it reads, so stale partials are harmless.
+// Dense workspace: a completion counter and the running maximum (FP32 bits;
+// each block folds its maximum in with one atomic max).  The caller zeroes
+// it once; the last block of every launch sets both back to zero, so
+// consecutive launches need no memset in between.  A stale counter c > 0 (a
+// workspace never zeroed) hands some block a ticket >= gridDim.x, which
+// records BSQ_ERR_VALUE; with c >= gridDim.x no block is last and nothing is
+// written, with a smaller c the block holding ticket gridDim.x - 1 may
+// finish before the remaining blocks have folded in their maxima (that
+// launch's outputs are reported as invalid).  A stale maximum under a zero
+// counter is not detected (as for the per-expert maxima of the grouped
+// workspace): the workspace must be zeroed whole.  The rest of the
+// workspace (its size is part of the interface) is unused.
 struct AmaxWorkspace {
   unsigned int counter;
-  unsigned int pad[3];
-  unsigned int partial[kAmaxMaxBlocks];
+  unsigned int amax_bits;
+  unsigned int pad[2];
+  unsigned int unused[kAmaxMaxBlocks];
 };
 
 __device__ __forceinline__ float tensor_sf_of(float amax) {
@@ -90,7 +94,7 @@ __global__ void __launch_bounds__(kAmaxThreads)
   if (threadIdx.x == 0) {
     uint32_t bm = 0;
     for (int w = 0; w < kAmaxWarps; ++w) bm = max(bm, warp_max[w]);
-    ws->partial[blockIdx.x] = bm;
+    if (bm != 0u) atomicMax(&ws->amax_bits, bm);  // non-negative FP32 maxima order like their bits
     __threadfence();
     const unsigned int ticket = atomicAdd(&ws->counter, 1u);
     if (ticket >= gridDim.x) record_error(kErrValue);
@@ -98,17 +102,11 @@ __global__ void __launch_bounds__(kAmaxThreads)
   }
   __syncthreads();
   if (!last) return;
-  // last block: reduce every block's partial
+  // last block: every block's maximum is in
   __threadfence();
-  uint32_t bm = 0;
-  for (int b = threadIdx.x; b < static_cast<int>(gridDim.x); b += kAmaxThreads)
-    bm = max(bm, __ldcg(ws->partial + b));
-  bm = warp_max_bits(bm);
-  if (lane == 0) warp_max[warp] = bm;
-  __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t m = 0;
-    for (int w = 0; w < kAmaxWarps; ++w) m = max(m, warp_max[w]);
+    const uint32_t m = __ldcg(&ws->amax_bits);
+    ws->amax_bits = 0u;
     const float amax = __uint_as_float(m);
     out[0] = amax;
     out[1] = tensor_sf_of(amax);

@@ -279,7 +279,9 @@ BSQ_API int32_t bsq_quantize_dynamic(int32_t fmt, const void* in_dev, int64_t M,
  *                 written; a smaller stale value can let a block finish the
  *                 reduction before the others have arrived, so the outputs of
  *                 a launch that reported BSQ_ERR_VALUE must be discarded.  A
- *                 workspace left non-zero must be zeroed again before reuse.
+ *                 stale running maximum under a zero counter is NOT detected
+ *                 (it would be folded into amax): a workspace left non-zero
+ *                 must be zeroed whole before reuse.
  *                 Calls sharing one workspace must not overlap on the GPU.
  *   The reduction reads in_dev with an L2 evict_last hint, so that a quantize
  *   of the same tensor right after it finds much of it in L2; that quantize
