@@ -204,7 +204,9 @@ BSQ_API int64_t bsq_grouped_quantize_workspace_bytes(int32_t fmt, int64_t total_
 
 /*
  * bsq_grouped_quantize_kernel with a caller workspace for the token kernel's
- * NVFP4 scales.  The token kernel (BSQ_GROUPED_TOKEN, or AUTO choosing it)
+ * NVFP4 scales (an extension; the pages' grouped kernel writes its scales
+ * through TMA stores of whole tiles, which a token-major kernel cannot
+ * form).  The token kernel (BSQ_GROUPED_TOKEN, or AUTO choosing it)
  * then writes each destination row's scale bytes row-major into the
  * workspace (whole sectors instead of 4 bytes in each of 8 atoms) and a
  * second kernel moves the rows it wrote to their 5D positions with
