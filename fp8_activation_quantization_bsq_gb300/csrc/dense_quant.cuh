@@ -88,7 +88,6 @@ __global__ void __launch_bounds__(kDenseThreads)
         if (col0 + kDenseBoxCols < a.K) tma_prefetch_2d(&tmap, col0 + kDenseBoxCols, mt * kDenseTileRows);
       }
       pdl_wait();
-      pdl_trigger();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_parity = 0;  // per-stage bit masks
@@ -113,6 +112,9 @@ __global__ void __launch_bounds__(kDenseThreads)
           phase ^= 1u;
         }
       }
+      // the next kernel may launch once every tile load is issued (earlier,
+      // its blocks would sit beside these CTAs for the whole launch)
+      pdl_trigger();
       // Never leave the CTA with a TMA write still landing in shared memory.
       for (int s = 0; s < STAGES; ++s)
         if ((used >> s) & 1u)
