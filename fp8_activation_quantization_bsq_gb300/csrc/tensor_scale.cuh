@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kAmaxThreads)
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kAmaxWarps + warp; r < M;
        r += static_cast<int64_t>(gridDim.x) * kAmaxWarps)
     acc = absmax2(acc, row_absmax(in + r * ld, K, lane, pol));
+  pdl_trigger();  // this block's reads are done: the next kernel may launch
   const uint32_t wm = warp_max_bits(__float_as_uint(absmax_final(acc)));
   if (lane == 0) warp_max[warp] = wm;
   __syncthreads();
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
         warp_max_bits(__float_as_uint(absmax_final(row_absmax(a.in + src * a.ld_in, a.K, lane, pol))));
     if (lane == 0 && m != 0u) atomicMax(a.amax_bits + e, m);
   }
+  pdl_trigger();  // this block's reads are done: the next kernel may launch
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -326,6 +328,7 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAtThreads,
   __syncthreads();
   for (int i = threadIdx.x; i < a.G; i += kAtThreads)
     if (sh.gmax[i] != 0u) atomicMax(a.amax_bits + sh.e[i], sh.gmax[i]);
+  pdl_trigger();  // this block's reads are done: the next kernel may launch
   __syncthreads();
   cluster_sync_all();  // no block leaves while another may read its rowmax
   if (threadIdx.x == 0) {
