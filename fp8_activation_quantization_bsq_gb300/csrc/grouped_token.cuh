@@ -629,9 +629,6 @@ __global__ void __launch_bounds__(kTqThreads, 1) grouped_token_kernel(const Grou
     __syncwarp();
   }
 
-  // the next kernel may launch once the blocks' main work is done (it waits
-  // for this grid's completion before touching memory)
-  pdl_trigger();
   // (4) tokens with more destination rows than a bucket holds: re-scan and
   // quantize each of their rows on its own (warp-collective).
   __syncthreads();
