@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(kAmaxThreads) grouped_amax_kernel(const Groupe
 // rows, e.g. top-k routing).  A cluster of kAtCluster blocks owns
 // kAtCluster * kAtTokens consecutive source rows: each block reduces the max
 // |x| of its kAtTokens rows once (one warp per row) into shared memory; then
-// each block of the cluster scans its contiguous share of row_indices, and
+// each block of the cluster scans its contiguous share of row_indices (the
+// entries to visit compacted per warp and shared out over its lanes), and
 // each destination row whose source row the cluster owns folds that row's
 // maximum (read from the owning block's shared memory) into a per-group
 // maximum in shared memory; the block then issues one atomic max per group
@@ -201,11 +202,15 @@ constexpr int kAtCluster = 8;
 constexpr int kAtClusterTokens = kAtCluster * kAtTokens;
 constexpr int kAtMaxGroups = 1024;
 
+constexpr int kAtScanU = 2;  // 16-byte row_indices loads in flight per thread
 struct AtShared {
   uint32_t ro[kAtMaxGroups + 1];
   int32_t e[kAtMaxGroups];
   uint32_t gmax[kAtMaxGroups];  // per-group maximum found by this block's scan
   uint32_t rowmax[kAtTokens];
+  // per warp, one scan iteration's entries to visit (destination offset, source row)
+  uint32_t hit_d[kAtThreads / 32][32 * 4 * kAtScanU];
+  int32_t hit_s[kAtThreads / 32][32 * 4 * kAtScanU];
 };
 
 // max |x| over one row (K % 8 == 0): eight 16-byte loads in flight per lane,
@@ -278,7 +283,7 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAtThreads,
   const int64_t share = (nvec + kAtCluster - 1) / kAtCluster;
   const int64_t vb = share * rank;
   const int64_t ve = vb + share < nvec ? vb + share : nvec;
-  constexpr int U = 2;  // 16-byte loads in flight per thread
+  constexpr int U = kAtScanU;
   int4 q[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
@@ -311,15 +316,46 @@ __global__ void __cluster_dims__(kAtCluster, 1, 1) __launch_bounds__(kAtThreads,
         q[u] = v < ve ? __ldg(body + v) : make_int4(0, 0, 0, 0);
       }
     }
+    // The entries at_visit does not skip at once are compacted per warp and
+    // shared out over its lanes: row_indices lists each group's rows in
+    // token order, so a cluster's hits come in runs that would otherwise
+    // fall to a few lanes, each paying a search and a remote load per hit.
+    uint32_t hm = 0u;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t v = v0 + threadIdx.x + u * kAtThreads;
       if (v >= ve) continue;
-      const int64_t d = head + 4 * v;
-      at_visit(a, sh, c0, first_cluster, d, q[u].x);
-      at_visit(a, sh, c0, first_cluster, d + 1, q[u].y);
-      at_visit(a, sh, c0, first_cluster, d + 2, q[u].z);
-      at_visit(a, sh, c0, first_cluster, d + 3, q[u].w);
+      const int32_t s4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool bad = s4[e] < 0 || s4[e] >= a.in_rows;
+        const int64_t k = static_cast<int64_t>(s4[e]) - c0;
+        if (bad ? first_cluster : (k >= 0 && k < kAtClusterTokens)) hm |= 1u << (4 * u + e);
+      }
+    }
+    const int nh = __popc(hm);
+    int incl = nh;  // inclusive prefix count over the warp's lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (total > 0) {  // warp-uniform
+      int pos = incl - nh;
+#pragma unroll
+      for (int b = 0; b < 4 * U; ++b) {
+        if ((hm >> b) & 1u) {
+          const int u = b >> 2, e = b & 3;
+          sh.hit_d[warp][pos] = static_cast<uint32_t>(4 * (threadIdx.x + u * kAtThreads) + e);  // d - (head + 4 v0)
+          sh.hit_s[warp][pos] = e == 0 ? q[u].x : e == 1 ? q[u].y : e == 2 ? q[u].z : q[u].w;
+          ++pos;
+        }
+      }
+      __syncwarp();
+      for (int i = lane; i < total; i += 32)
+        at_visit(a, sh, c0, first_cluster, head + 4 * v0 + sh.hit_d[warp][i], sh.hit_s[warp][i]);
+      __syncwarp();
     }
   }
   if (rank == 0)
