@@ -126,3 +126,43 @@ def test_graph_grouped_token_quantize(bsq, ws):
         np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
         np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
     assert bsq.device_error() == 0
+
+
+def test_graph_grouped_dynamic_chain(bsq):
+    """Per-expert tensor scales (the token-major reduction: a gather that
+    reuses source rows) feeding the grouped NVFP4 quantize from device
+    memory, captured once and replayed on new token rows: the workspace
+    leaves itself zeroed, so every replay computes fresh scales, and scales,
+    packed rows and scale bytes equal the oracle."""
+    d = wl.config_grouped_prefill(seed=63, tokens=700, K=512, num_experts=24, top_k=8)
+    E = 24
+    T, K = 700, 512
+    u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).cuda()
+    ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
+    eid = torch.from_numpy(d["expert_ids"]).cuda()
+    ridx = torch.from_numpy(d["row_indices"]).cuda()
+    x = torch.zeros((T, K), dtype=torch.bfloat16, device="cuda")
+    gws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(E), dtype=torch.uint8, device="cuda")
+    sf = bsq.grouped_tensor_sf(x, ro, eid, E, ridx, total_rows=d["total_rows"], workspace=gws)
+    kw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"])
+    out, sc = bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, **kw)   # set-up before capture
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        bsq.grouped_tensor_sf(x, ro, eid, E, ridx, total_rows=d["total_rows"], out=sf, workspace=gws)
+        bsq.grouped_quantize(x, "nvfp4", ro, so, eid, sf, ridx, out=out, scales=sc, **kw)
+    for seed in (1, 2, 3):
+        rng = np.random.Generator(np.random.PCG64(80 + seed))
+        bits = wl.dense_activations(rng, T, K, "rowlognormal")
+        _bits_to_dev(bits, x)
+        _, sf_ref = oracle.expert_tensor_sf(bits, d["row_offsets"], d["expert_ids"], E, d["row_indices"])
+        p_ref, pw, s_ref, sw = oracle.grouped_quantize("nvfp4", bits, d["row_offsets"], d["scales_offsets"],
+                                                       d["expert_ids"], sf_ref, d["row_indices"])
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(sf.cpu().numpy(), sf_ref)
+        np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
+        np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
+    assert int(gws.count_nonzero().item()) == 0
+    assert bsq.device_error() == 0
