@@ -198,8 +198,9 @@ __device__ __forceinline__ uint32_t e2m1_word(float2 p0, float2 p1, float2 p2, f
   return r;
 }
 
-__device__ __forceinline__ void st_global_u8(void* p, uint32_t v) {
-  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Scale-byte store with an L2 cache policy.
+__device__ __forceinline__ void st_global_u8_policy(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
 }
 __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
@@ -219,6 +220,13 @@ __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_
   const int S = a.K / SF;          // blocks with data
   const int S4 = a.kt_atoms * 4;   // blocks with a scale byte (the last atom's padding is 0x00)
   const bool vec32 = a.in_vec32 != 0;
+  // Scale bytes are stored with an L2 evict_last hint: each 32-byte sector of
+  // a 5D atom collects 4-byte pieces of 8 destination rows written by other
+  // warps and blocks at other times, and the hint keeps it in L2 until it is
+  // complete instead of letting it go back to memory partly written (the
+  // next ordinary read, e.g. the consuming matmul's, returns the lines to
+  // normal priority).
+  const uint64_t keep = l2_policy_evict_last();
 #pragma unroll 1
   for (int j = jb + lane; j - lane < je; j += 32) {
     TqChunk<FMT> nx;
@@ -264,7 +272,7 @@ __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_
 #pragma unroll
         for (int m = 0; m < 8; ++m) z[m] = __fmul2_rn(y[m], ff);
         if (has) st_global_v2(dd.out + el_off, e2m1_word(z[0], z[1], z[2], z[3]), e2m1_word(z[4], z[5], z[6], z[7]));
-        if (has_scale) st_global_u8(dd.scale + sc_off, b);
+        if (has_scale) st_global_u8_policy(dd.scale + sc_off, b, keep);
       }
     } else {
       const MxScale sc = mx_scale<FMT == kMXFP4 ? 6 : 448>(amax);
@@ -296,7 +304,7 @@ __device__ __forceinline__ void tq_row(const GroupedArgs& a, const uint16_t* in_
             st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
           }
         }
-        if (has_scale) st_global_u8(desc[i].scale + sc_off, sbyte);
+        if (has_scale) st_global_u8_policy(desc[i].scale + sc_off, sbyte, keep);
       }
     }
     cur = nx;

@@ -181,7 +181,10 @@ typedef enum {
 /*
  * bsq_grouped_quantize with an explicit kernel choice (bsq_grouped_kernel);
  * the results are identical whichever kernel runs.  An unknown `kernel`
- * returns BSQ_ERR_VALUE.
+ * returns BSQ_ERR_VALUE.  The token kernel stores scale bytes with an L2
+ * evict_last hint (their 32-byte sectors fill from many rows over the
+ * launch); the lines return to normal priority on their next ordinary read,
+ * e.g. by the matmul that consumes the scales.
  */
 BSQ_API int32_t bsq_grouped_quantize_kernel(int32_t fmt, const void* in_dev, int64_t in_rows,
                                             int64_t K, int64_t ld_in,
