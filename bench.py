@@ -21,8 +21,9 @@ Python API with pinned host buffers, host<->device copies inside the timed
 region), ``roofline`` for the dominant kernel (dense quantize), ``clocks``
 sampled with nvidia-smi during the timed region, ``cpu_baseline`` (the CPU
 oracle on a bounded sample, rank 0 at N=1) and ``workloads`` (the other
-shapes: NVFP4 128x256, MXFP8/MXFP4 16384x4096, grouped NVFP4 prefill, grouped
-decode in microseconds per k_tiles_per_block).
+shapes: NVFP4 128x256, MXFP8/MXFP4 16384x4096, grouped prefill with the
+top-8 gather and with the rows already permuted, grouped decode in
+microseconds per k_tiles_per_block, the tensor scales and the chains).
 
 ``--impl reference`` times the CPU oracle itself on the same workload, one
 bounded sample per step.
@@ -211,17 +212,21 @@ def gpu_hold(ms: float) -> None:
     torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
 
 
-def time_events(fn, reps: int, flush=None):
+def time_events(fn, reps: int, flush=None, prep=None):
     """Mean / min device ms of fn() over reps, CUDA events on the current
     stream.  With ``flush`` (a buffer of 2x the L2 size) a read pass over it
     runs before each rep, outside the events: it evicts earlier data and
-    writes back dirty lines, leaving L2 clean (cold-cache timing)."""
+    writes back dirty lines, leaving L2 clean (cold-cache timing).  ``prep``
+    (enqueued before the flush) reads what a consumer of the previous rep's
+    outputs would read."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     torch.cuda.synchronize()
     gpu_hold(1.0 + 0.15 * reps)
     for i, (a, b) in enumerate(evs):
+        if prep is not None:
+            prep()
         if flush is not None:
             flush.sum(dtype=torch.int32)
         a.record()
@@ -235,6 +240,13 @@ def time_events(fn, reps: int, flush=None):
 E2E_SLABS = 4       # row slabs of one end-to-end step (copies overlapped with the kernels)
 ROT_SETS = 3        # buffer sets cycled by the back-to-back context timings
 ROT_LAUNCHES = 30
+
+
+class ScaleList(list):
+    """A list of launch closures that also keeps their scale buffers."""
+    def __init__(self):
+        super().__init__()
+        self.scales = []
 
 
 def time_rotated(fns, launches: int = ROT_LAUNCHES):
@@ -353,21 +365,33 @@ def extra_workloads(bsq, device, flush, peak):
         del outs, fns
     del xs, x0
 
+    def consume(tensors):
+        # read the outputs once, as their consumer would: the grouped token
+        # and band kernels store scale bytes with an L2 evict_last hint, and
+        # an ordinary read returns those lines to normal priority, so that a
+        # workload's unread scales do not stay favoured in L2 through the
+        # workloads measured after it
+        for t in tensors:
+            t.max()
+        torch.cuda.synchronize()
+
     def grouped_sets(d, fmt, kt, sets, workspace=False):
         """Launch closures over `sets` buffer sets (token-matrix copy, packed
         output, 5D scales, optionally the scale-staging workspace; the
-        metadata shared) and the algorithmic bytes."""
+        metadata shared) and the algorithmic bytes; the sets' scale buffers
+        are kept in fns.scales."""
         x0 = to_dev_bf16(d["x_bits"], device)
         xgs = [x0] + [x0.clone() for _ in range(sets - 1)]
         u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
         ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
         eid = torch.from_numpy(d["expert_ids"]).to(device)
         sf = torch.from_numpy(d["sf_tensor"]).to(device) if fmt == "nvfp4" else None
-        ridx = torch.from_numpy(d["row_indices"]).to(device)
+        ridx = torch.from_numpy(d["row_indices"]).to(device) if d["row_indices"] is not None else None
         kw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=kt)
-        fns = []
+        fns = ScaleList()
         for xg in xgs:
             out, sc = bsq.grouped_quantize(xg, fmt, ro, so, eid, sf, ridx, **kw)
+            fns.scales.append(sc)
             ws = torch.empty(bsq.grouped_quantize_workspace_bytes(fmt, d["total_scale_rows"], d["K"]),
                              dtype=torch.uint8, device=device) if workspace else None
             fns.append(lambda xg=xg, out=out, sc=sc, ws=ws: bsq.grouped_quantize(
@@ -375,9 +399,10 @@ def extra_workloads(bsq, device, flush, peak):
         K = d["K"]
         sfv = 16 if fmt == "nvfp4" else 32
         kt_cols = -(-(K // sfv) // 4) * 4
-        uniq = int(np.unique(d["row_indices"]).size)
+        gather = d["row_indices"] is not None
+        uniq = int(np.unique(d["row_indices"]).size) if gather else d["total_rows"]
         b = (uniq * K * 2 + d["total_rows"] * (K if fmt == "mxfp8" else K // 2)
-             + d["total_rows"] * kt_cols + d["row_indices"].nbytes + d["row_offsets"].nbytes
+             + d["total_rows"] * kt_cols + (d["row_indices"].nbytes if gather else 0) + d["row_offsets"].nbytes
              + d["scales_offsets"].nbytes + d["expert_ids"].nbytes
              + (d["sf_tensor"].nbytes if fmt == "nvfp4" else 0))
         return fns, b
@@ -409,7 +434,7 @@ def extra_workloads(bsq, device, flush, peak):
         bsq.grouped_quantize(xgs[i], "nvfp4", ro, so_d, eid, gsfs[i], ridx, out=gouts[i][0], scales=gouts[i][1],
                              **gkw)
     rot = time_rotated([lambda i=i: gchain(i) for i in range(ROT_SETS)])
-    single, _ = time_events(lambda: gchain(0), reps, flush)
+    single, _ = time_events(lambda: gchain(0), reps, flush, prep=lambda: gouts[0][1].max())
     res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168"] = {"us": round(rot * 1e3, 2),
                                                              "us_single_cold": round(single * 1e3, 2)}
     # the same chain with the quantize's scale-staging workspace
@@ -423,29 +448,45 @@ def extra_workloads(bsq, device, flush, peak):
     rot = time_rotated([lambda i=i: gchain_ws(i) for i in range(ROT_SETS)])
     res["nvfp4_grouped_dynamic_chain_prefill_T4096_K7168_workspace"] = {"us": round(rot * 1e3, 2)}
     del gwss
+    consume([g[1] for g in gouts])
     del gouts, so_d, xgs, x0, gsfs, gws, fns
     for fmt, ws in (("nvfp4", False), ("nvfp4", True), ("mxfp8", False), ("mxfp4", False)):
         fns, b = grouped_sets(d, fmt, 8, ROT_SETS, workspace=ws)
         rot = time_rotated(fns)
-        single, _ = time_events(fns[0], reps, flush)
+        single, _ = time_events(fns[0], reps, flush, prep=lambda: fns.scales[0].max())
         res[f"{fmt}_grouped_prefill_T4096_K7168" + ("_workspace" if ws else "")] = {
             "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
             "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
             "algorithmic_bytes": b, "logical_input_bytes": d["total_rows"] * d["K"] * 2,
             "T_elements_per_s": round(d["total_rows"] * d["K"] / (rot * 1e-3) / 1e12, 2)}
+        consume(fns.scales)
         del fns
-    del d
+    # the same groups with the rows already permuted (row_indices NULL: the
+    # 32768 x 7168 input is read once, row by row)
+    dn = dict(d, x_bits=d["x_bits"][d["row_indices"]], row_indices=None)
+    for fmt in ("nvfp4", "mxfp8", "mxfp4"):
+        fns, b = grouped_sets(dn, fmt, 8, ROT_SETS)
+        rot = time_rotated(fns)
+        single, _ = time_events(fns[0], reps, flush, prep=lambda: fns.scales[0].max())
+        res[f"{fmt}_grouped_prefill_nogather_R32768_K7168"] = {
+            "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
+            "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
+            "algorithmic_bytes": b, "note": "rows already permuted by expert (no row_indices)"}
+        consume(fns.scales)
+        del fns
+    del d, dn
     for fmt in ("nvfp4", "mxfp8"):
         for K in (7168, 2048):
             d = wl.config_grouped_decode(K=K, fmt=fmt)
             for kt in (0, 1, 2, 4, 8):  # 0: chosen by the library
                 fns, b = grouped_sets(d, fmt, kt, 1)
-                mean, mn = time_events(fns[0], reps, flush)
+                mean, mn = time_events(fns[0], reps, flush, prep=lambda: fns.scales[0].max())
                 warm = time_events(fns[0], reps)[0]
                 b2b = time_rotated(fns)
                 res[f"{fmt}_grouped_decode_T64_K{K}_kt{'auto' if kt == 0 else kt}"] = {
                     "us_single_cold": round(mean * 1e3, 2), "us_min": round(mn * 1e3, 2),
                     "us_single_warm_l2": round(warm * 1e3, 2), "us_back_to_back_warm_l2": round(b2b * 1e3, 2)}
+                consume(fns.scales)
                 del fns
     return res
 

@@ -237,7 +237,15 @@ __device__ __forceinline__ void band_chunk_step(const uint4 (&v)[4], int ch, int
   uint32_t word = bytes << (8 * BPL * (lane % CPA));
 #pragma unroll
   for (int m = 1; m < CPA; m <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, m);
-  if (lane % CPA == 0 && ch < c_end) *reinterpret_cast<uint32_t*>(scale_row + (ch / CPA) * 512) = word;
+  // (the atom's 32-byte sectors fill from rows of 4 blocks: kept in L2 until
+  // complete by an evict_last hint; the next ordinary read returns them to
+  // normal priority)
+  if (lane % CPA == 0 && ch < c_end) {
+    const uint64_t keep = l2_policy_evict_last();
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(scale_row + (ch / CPA) * 512), "r"(word),
+                 "l"(keep)
+                 : "memory");
+  }
 }
 
 // A block owns kBdRows consecutive destination rows (across group boundaries)
