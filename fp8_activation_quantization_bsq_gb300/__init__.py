@@ -15,7 +15,8 @@ Operations (Modular "block_scaled_quantization" pages):
   block_scaled_dot    -- the idea of naive_block_scaled_matmul (a validator)
 and the steps around them: tensor_sf / grouped_tensor_sf (the NVFP4 tensor
 scales on the GPU), quantize_dynamic (tensor_sf read from device memory),
-gemm_quantize (a matmul with the quantize in its epilogue).
+grouped_quantize_dynamic (per-expert scales on the GPU, then the grouped
+quantize), gemm_quantize (a matmul with the quantize in its epilogue).
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ from ._build import LIB_PATH
 
 __all__ = ["FORMATS", "GROUPED_KERNELS", "lib", "BsqError", "block_size", "packed_row_bytes",
            "scales5d_bytes", "quantize", "quantize_dynamic", "tensor_sf", "grouped_tensor_sf",
+           "grouped_quantize_dynamic",
            "grouped_quantize", "grouped_quantize_workspace_bytes", "scales_interleave", "block_scaled_dot", "gemm_quantize", "device_error",
            "status_string"]
 
@@ -266,6 +268,31 @@ def grouped_quantize(x: torch.Tensor, fmt, row_offsets, scales_offsets, expert_i
             _stream(x.device, stream))
     _check(rc, "bsq_grouped_quantize")
     return out, scales
+
+
+def grouped_quantize_dynamic(x: torch.Tensor, row_offsets, scales_offsets, expert_ids, num_experts: int,
+                             row_indices=None, total_rows: int | None = None,
+                             total_scale_rows: int | None = None, k_tiles_per_block: int = 0,
+                             out=None, scales=None, sf_out=None, tsf_workspace=None, workspace=None,
+                             stream=None, kernel: str = "auto"):
+    """Grouped NVFP4 quantize with the per-expert tensor scales computed on
+    the GPU first (``grouped_tensor_sf``) and read by the quantize from
+    device memory, both on one stream with nothing waiting for the host.
+    ``tsf_workspace``: the scales' reduction workspace (zeroed once, left
+    zeroed; allocated when None); ``workspace``: as for
+    :func:`grouped_quantize`.  Returns (packed, scales, sf_tensor
+    float32 [num_experts])."""
+    if total_rows is None:
+        if out is None:
+            raise ValueError("total_rows is required when out is not given")
+        total_rows = out.shape[0]
+    sf = grouped_tensor_sf(x, row_offsets, expert_ids, num_experts, row_indices, total_rows=total_rows,
+                           out=sf_out, workspace=tsf_workspace, stream=stream)
+    packed, sc = grouped_quantize(x, "nvfp4", row_offsets, scales_offsets, expert_ids, sf, row_indices,
+                                  total_rows=total_rows, total_scale_rows=total_scale_rows,
+                                  k_tiles_per_block=k_tiles_per_block, out=out, scales=scales, stream=stream,
+                                  kernel=kernel, workspace=workspace)
+    return packed, sc, sf
 
 
 def grouped_quantize_workspace_bytes(fmt, total_scale_rows: int, K: int) -> int:

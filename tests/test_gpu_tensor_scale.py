@@ -250,3 +250,23 @@ def test_stale_counter_is_reported(bsq, stale):
     assert bsq.device_error() == 4
     if stale >= 1024:
         assert np.all(_f32(gout) == -7.0)
+
+
+@pytest.mark.parametrize("kernel", ["auto", "token"])
+def test_grouped_quantize_dynamic_matches_oracle(bsq, kernel):
+    """One call: per-expert scales on the GPU, then the grouped NVFP4
+    quantize reading them from device memory."""
+    d = wl.config_grouped_prefill(seed=9, tokens=400, K=1024, num_experts=32, top_k=8)
+    E = 32
+    x = to_device_bf16(d["x_bits"])
+    ro, so = u32_device(d["row_offsets"]), u32_device(d["scales_offsets"])
+    eid, ridx = i32_device(d["expert_ids"]), i32_device(d["row_indices"])
+    out, sc, sf = bsq.grouped_quantize_dynamic(x, ro, so, eid, E, ridx, total_rows=d["total_rows"],
+                                               total_scale_rows=d["total_scale_rows"], kernel=kernel)
+    _, sf_ref = oracle.expert_tensor_sf(d["x_bits"], d["row_offsets"], d["expert_ids"], E, d["row_indices"])
+    p_ref, pw, s_ref, sw = oracle.grouped_quantize("nvfp4", d["x_bits"], d["row_offsets"], d["scales_offsets"],
+                                                   d["expert_ids"], sf_ref, d["row_indices"])
+    np.testing.assert_array_equal(sf.cpu().numpy(), sf_ref)
+    np.testing.assert_array_equal(out.cpu().numpy()[pw], p_ref[pw])
+    np.testing.assert_array_equal(sc.cpu().numpy()[sw], s_ref[sw])
+    assert bsq.device_error() == 0
