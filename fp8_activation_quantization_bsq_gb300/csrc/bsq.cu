@@ -427,7 +427,12 @@ int32_t bsq_tensor_sf(const void* in, int64_t M, int64_t K, int64_t ld_in, float
   AmaxWorkspace* ws = static_cast<AmaxWorkspace*>(workspace);
   const int64_t rows = (M > 0 && K > 0) ? M : 0;
   int64_t grid = ceil_div(rows, kAmaxWarps);
-  const int64_t cap = std::min<int64_t>(kAmaxMaxBlocks, static_cast<int64_t>(d->sm_count) * 4);
+  // up to 8 blocks per SM (a warp per row on 8192 x 7168): with all rows in
+  // flight at once the quantize that follows finds more of them in L2 (the
+  // reads carry evict_last); the reduction alone is faster with 4 per SM
+  // (20.3 against 22.5 us) but the tensor_sf -> quantize chain, its use, is
+  // not (51.8 against 46.4 us)
+  const int64_t cap = std::min<int64_t>(kAmaxMaxBlocks, static_cast<int64_t>(d->sm_count) * 8);
   grid = std::max<int64_t>(1, std::min(grid, cap));
   const cudaError_t e = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(grid)),
                                    dim3(kAmaxThreads), 0, st, static_cast<const uint16_t*>(in), rows,
