@@ -22,7 +22,8 @@ region), ``roofline`` for the dominant kernel (dense quantize), ``clocks``
 sampled with nvidia-smi during the timed region, ``cpu_baseline`` (the CPU
 oracle on a bounded sample, rank 0 at N=1) and ``workloads`` (the other
 shapes: NVFP4 128x256, MXFP8/MXFP4 16384x4096, grouped prefill with the
-top-8 gather and with the rows already permuted, grouped decode in
+top-8 gather and with the rows already permuted (32768 and 8192 rows),
+grouped decode in
 microseconds per k_tiles_per_block, the tensor scales and the chains).
 
 ``--impl reference`` times the CPU oracle itself on the same workload, one
@@ -472,6 +473,21 @@ def extra_workloads(bsq, device, flush, peak):
             "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
             "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
             "algorithmic_bytes": b, "note": "rows already permuted by expert (no row_indices)"}
+        consume(fns.scales)
+        del fns
+    del d, dn
+    # fewer rows without a gather (1024 tokens, top-8 of 256 experts, rows
+    # permuted): the streaming kernel splits its column runs to fill the GPU
+    d = wl.config_grouped_prefill(seed=11, tokens=1024, K=7168)
+    dn = dict(d, x_bits=d["x_bits"][d["row_indices"]], row_indices=None)
+    for fmt in ("nvfp4", "mxfp8", "mxfp4"):
+        fns, b = grouped_sets(dn, fmt, 8, ROT_SETS)
+        rot = time_rotated(fns)
+        single, _ = time_events(fns[0], reps, flush, prep=lambda: fns.scales[0].max())
+        res[f"{fmt}_grouped_nogather_R8192_K7168"] = {
+            "GB_s": round(b / (rot * 1e6), 1), "us": round(rot * 1e3, 2),
+            "frac_of_hbm": round(b / (rot * 1e6) / peak, 3), "us_single_cold": round(single * 1e3, 2),
+            "algorithmic_bytes": b, "note": "1024 tokens top-8, rows already permuted (no row_indices)"}
         consume(fns.scales)
         del fns
     del d, dn
