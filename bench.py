@@ -842,7 +842,8 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-CASES = ("grouped_prefill", "grouped_decode", "tensor_sf", "grouped_tensor_sf", "mxfp8", "mxfp4", "gemm_quantize")
+CASES = ("grouped_prefill", "grouped_nogather", "grouped_decode", "tensor_sf", "grouped_tensor_sf", "mxfp8", "mxfp4",
+         "gemm_quantize")
 
 
 def run_case(args):
@@ -854,14 +855,16 @@ def run_case(args):
     import workloads as wl
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    if args.case in ("grouped_prefill", "grouped_decode", "grouped_tensor_sf"):
+    if args.case in ("grouped_prefill", "grouped_nogather", "grouped_decode", "grouped_tensor_sf"):
         d = wl.config_grouped_prefill() if args.case != "grouped_decode" else wl.config_grouped_decode()
+        if args.case == "grouped_nogather":  # the same groups with the rows already permuted
+            d = dict(d, x_bits=d["x_bits"][d["row_indices"]], row_indices=None)
         x = to_dev_bf16(d["x_bits"], device)
         u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint32).view(np.int32)).to(device)
         ro, so = u32(d["row_offsets"]), u32(d["scales_offsets"])
         eid = torch.from_numpy(d["expert_ids"]).to(device)
         sf = torch.from_numpy(d["sf_tensor"]).to(device)
-        ridx = torch.from_numpy(d["row_indices"]).to(device)
+        ridx = torch.from_numpy(d["row_indices"]).to(device) if d["row_indices"] is not None else None
         kw = dict(total_rows=d["total_rows"], total_scale_rows=d["total_scale_rows"], k_tiles_per_block=8)
         if args.case == "grouped_tensor_sf":
             ws = torch.zeros(bsq.lib().bsq_grouped_tensor_sf_workspace_bytes(d["num_experts"]),
