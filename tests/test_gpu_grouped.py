@@ -600,3 +600,13 @@ def test_grouped_workspace_bad_source_rows_reported(bsq):
     good[bad] = False
     np.testing.assert_array_equal(p[good], p_ref[good])
     assert np.all(p[bad] == SENTINEL)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8", "mxfp4"])
+def test_grouped_stream_split_runs_gathered_K7168(bsq, fmt):
+    """The streaming kernel on a gathered 8192-row routing (1024 tokens,
+    top-8 of 256 experts, K = 7168): few rows, so each block's run of
+    columns is split into seven; every written byte against the oracle."""
+    d = wl.config_grouped_prefill(seed=11, tokens=1024, K=7168, fmt=fmt)
+    p, s = _run_grouped(bsq, fmt, d, 0, kernel="stream")
+    _compare(fmt, d, p, s)
