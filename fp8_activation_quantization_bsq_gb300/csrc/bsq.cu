@@ -205,7 +205,8 @@ bsq_status launch_grouped_band(GroupedArgs a, cudaStream_t stream) {
   // 16384 rows 64.0 -> 54.5 us, 32768 rows 103.6 -> 102.2 us (MXFP8 115.6 ->
   // 108.1 us); six blocks per SM instead gave 18.2 / 32.2 / 64.0 / 103.6 us.
   a.ktc = kBdChunksPerBlock;
-  while (a.ktc > 32 && blocks * ceil_div(c_pad, static_cast<int64_t>(a.ktc)) < 12 * static_cast<int64_t>(d->sm_count))
+  while (a.ktc > 32 && blocks * ceil_div(c_pad, static_cast<int64_t>(a.ktc)) < 12 * static_cast<int64_t>(d->sm_count) &&
+         ceil_div(c_pad, static_cast<int64_t>(a.ktc - 32)) <= 65535)  // the grid's y extent
     a.ktc -= 32;
   const int64_t chunks = ceil_div(c_pad, a.ktc);
   if (chunks > 65535 || blocks >= (int64_t(1) << 31)) return BSQ_ERR_SHAPE;
